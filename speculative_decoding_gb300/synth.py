@@ -1,0 +1,186 @@
+"""Seeded synthetic inputs for the XPress Jacobi pass.
+
+This module only draws random data: it holds none of the pass's arithmetic
+(no argmax, no matmul, no mixer), so both the CUDA path and the CPU oracle can
+be fed from it.  Trained weights and real hidden states are not available, so
+the distributions below stand in for them (all from one seed per workload):
+
+  E[V, D]            bf16  ~ N(0, 0.02)               token embedding
+  W_lat[D, R]        bf16  ~ N(0, 1/sqrt(D))          [in, out]
+  Wg, Wu[R, H]       bf16  ~ N(0, 1/sqrt(R))
+  Wd[H, R]           bf16  ~ N(0, 1/sqrt(H))
+  W2[R, V]           bf16  ~ N(0, 1/sqrt(R))
+  L[B, B, R]         fp32  lower-triangular ~ U(0, 1), each (b, r) row
+                           normalised to sum 1 over j <= b (the folded mixer)
+  hcache[N, B, R]    bf16  ~ N(0, 1)
+  base[N*(B-1), V]   bf16  ~ N(0, 3)
+  bias[N*(B-1), V]   bf16  ~ N(0, 1)                 (standalone add-argmax)
+  am1[N], blk[N, B]  int64 ~ U[0, V)
+
+N(0, s) names the standard deviation s.  bf16 tensors are returned as numpy
+``uint16`` bit patterns (converted from fp32 with torch's round-to-nearest-even
+cast); tokens as ``int64``; L as ``float32``.
+
+Normals come from numpy's Philox generator in fixed chunks, one child seed per
+chunk, so the values do not depend on the number of threads used.
+"""
+
+from __future__ import annotations
+
+import math
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+_CHUNK = 1 << 22
+
+
+@dataclass(frozen=True)
+class PassShape:
+    """One workload of the pass: N blocks of B slots, vocab V, embedding width
+    D, latent rank R, MLP hidden H, and its seed."""
+
+    name: str
+    N: int
+    B: int
+    V: int
+    D: int
+    R: int
+    H: int
+    seed: int
+
+    @property
+    def rows(self) -> int:
+        return self.N * (self.B - 1)
+
+
+# Workloads, named by what they are.
+TINY = PassShape("tiny N=2 B=4 V=1000 D=64 R=32 H=64", 2, 4, 1000, 64, 32, 64, seed=0)
+SERVE = PassShape("pass N=32 B=16 V=152064 D=3584 R=512 H=1536", 32, 16, 152064, 3584, 512, 1536, seed=2)
+FLOOR = PassShape("pass N=1 B=16 V=152064 D=3584 R=512 H=1536", 1, 16, 152064, 3584, 512, 1536, seed=3)
+FIXPOINT = PassShape("fixpoint N=64 B=16 V=152064 D=3584 R=512 H=1536", 64, 16, 152064, 3584, 512, 1536, seed=4)
+
+ARGMAX_ROWS, ARGMAX_V, ARGMAX_SEED = 480, 152064, 1   # rows = 32 * 15
+
+
+def _threads() -> int:
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+def _normal_f32(seed: int, stream: int, n: int, std: float) -> np.ndarray:
+    out = np.empty(n, np.float32)
+    nchunks = max(1, (n + _CHUNK - 1) // _CHUNK)
+    kids = np.random.SeedSequence([seed, stream]).spawn(nchunks)
+    s = np.float32(std)
+
+    def work(i: int) -> None:
+        lo, hi = i * _CHUNK, min(n, (i + 1) * _CHUNK)
+        if hi > lo:
+            g = np.random.Generator(np.random.Philox(kids[i]))
+            g.standard_normal(hi - lo, dtype=np.float32, out=out[lo:hi])
+            out[lo:hi] *= s
+
+    if nchunks == 1:
+        work(0)
+    else:
+        with ThreadPoolExecutor(_threads()) as ex:
+            list(ex.map(work, range(nchunks)))
+    return out
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 numpy -> bf16 bit patterns (uint16), torch's RNE cast."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def normal_bf16(seed: int, stream: int, shape, std: float) -> np.ndarray:
+    n = int(np.prod(shape))
+    return to_bf16_bits(_normal_f32(seed, stream, n, std)).reshape(shape)
+
+
+def tokens(seed: int, stream: int, shape, V: int) -> np.ndarray:
+    g = np.random.Generator(np.random.Philox(np.random.SeedSequence([seed, stream])))
+    return g.integers(0, V, size=shape, dtype=np.int64)
+
+
+def mixer(seed: int, B: int, R: int) -> np.ndarray:
+    """L[b, j, r]: U(0,1) for j <= b, 0 above the diagonal, each (b, r) row
+    scaled to sum 1 over j."""
+    g = np.random.Generator(np.random.Philox(np.random.SeedSequence([seed, 7])))
+    u = g.random((B, B, R), dtype=np.float64)
+    tri = np.tril(np.ones((B, B)))[:, :, None]
+    u = u * tri
+    u = u / u.sum(axis=1, keepdims=True)
+    return u.astype(np.float32)
+
+
+# stream ids, fixed per tensor
+_S = dict(E=1, W_lat=2, Wg=3, Wu=4, Wd=5, W2=6, hcache=8, base=9, bias=10, am1=11, blk=12)
+
+
+def pass_inputs(shape: PassShape, with_embedding: bool = True) -> dict:
+    """All inputs of one pass.  ``with_embedding=False`` skips E (the largest
+    tensor) for callers that build it elsewhere."""
+    s, N, B, V, D, R, H = shape.seed, shape.N, shape.B, shape.V, shape.D, shape.R, shape.H
+    out = dict(
+        W_lat=normal_bf16(s, _S["W_lat"], (D, R), 1.0 / math.sqrt(D)),
+        L=mixer(s, B, R),
+        Wg=normal_bf16(s, _S["Wg"], (R, H), 1.0 / math.sqrt(R)),
+        Wu=normal_bf16(s, _S["Wu"], (R, H), 1.0 / math.sqrt(R)),
+        Wd=normal_bf16(s, _S["Wd"], (H, R), 1.0 / math.sqrt(H)),
+        W2=normal_bf16(s, _S["W2"], (R, V), 1.0 / math.sqrt(R)),
+        hcache=normal_bf16(s, _S["hcache"], (N, B, R), 1.0),
+        base=normal_bf16(s, _S["base"], (N * (B - 1), V), 3.0),
+        am1=tokens(s, _S["am1"], (N,), V),
+        blk=tokens(s, _S["blk"], (N, B), V),
+    )
+    if with_embedding:
+        out["E"] = normal_bf16(s, _S["E"], (V, D), 0.02)
+    return out
+
+
+def plant_ties(base: np.ndarray, bias: np.ndarray, frac: float, seed: int, min_rows: int = 1):
+    """Plant duplicated row maxima, in place.
+
+    For round(frac * rows) rows (at least ``min_rows`` when frac > 0), 2 to 4
+    random positions get base = a value above max(base[row]) + max(bias[row]) + 1
+    and bias = 0, so those positions hold the row's strict maximum and tie with
+    each other; the lowest of them is the expected answer by construction.
+    Returns {row: sorted positions}."""
+    rows, V = base.shape
+    k = int(round(frac * rows))
+    if frac > 0:
+        k = max(k, min_rows)
+    k = min(k, rows)
+    g = np.random.Generator(np.random.Philox(np.random.SeedSequence([seed, 99])))
+    chosen = sorted(g.choice(rows, size=k, replace=False).tolist()) if k else []
+    planted = {}
+    for r in chosen:
+        bmax = float(np.max(_f32(base[r]))) + float(np.max(_f32(bias[r]))) + 1.0
+        top = to_bf16_bits(np.array([bmax], np.float32))[0]
+        if _f32(np.array([top]))[0] <= bmax - 1.0:   # cannot happen for these ranges
+            raise AssertionError("planted value does not exceed the row")
+        cnt = int(g.integers(2, 5))
+        pos = np.sort(g.choice(V, size=min(cnt, V), replace=False))
+        base[r, pos] = top
+        bias[r, pos] = 0
+        planted[r] = pos.tolist()
+    return planted
+
+
+def _f32(h: np.ndarray) -> np.ndarray:
+    return (np.asarray(h, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def argmax_inputs(rows: int, V: int, N: int, B: int, seed: int, tie_frac: float):
+    """Standalone add-argmax inputs: base ~N(0,3), bias ~N(0,1), [rows, V]
+    row-contiguous, plus a block buffer and the planted-tie rows."""
+    base = normal_bf16(seed, _S["base"], (rows, V), 3.0)
+    bias = normal_bf16(seed, _S["bias"], (rows, V), 1.0)
+    planted = plant_ties(base, bias, tie_frac, seed)
+    blk = tokens(seed, _S["blk"], (N, B), V)
+    return dict(base=base, bias=bias, blk=blk, planted=planted)
