@@ -1,0 +1,167 @@
+/*
+ * xpress.h -- C ABI of libxpress.so: one XPress Jacobi draft pass on one
+ * NVIDIA GB300 (sm_103a) GPU.
+ *
+ * The method (vLLM docs, module "vllm.v1.worker.gpu.spec_decode.xpress.kernels",
+ * module docstring): a pass over N blocks of B slots (slot 0 is the verified
+ * anchor) computes
+ *     latent   u[n,b,:] = causal_mix(hcache[n,b] + E[prev[n,b]] @ W_lat)
+ *              x[n,b,:] = u[n,b,:] + SwiGLU_MLP(u[n,b,:])
+ *     readout  logits[r,:] = base[r,:] + x[n,1+j,:] @ W2      r = n*(B-1)+j
+ *     argmax   blk[n,1+j] = argmax_v logits[r,v]
+ * and never stores the [N*(B-1), V] logits.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers named d_* are DEVICE pointers owned by the caller.  The library
+ *   allocates no device memory, never synchronises the device and only
+ *   enqueues work on `stream` (0 = the legacy default stream).
+ * - bf16 data is passed as xp_bf16 (the 16-bit pattern of a bfloat16).  Tokens
+ *   are int64.  The mixer L is float32.
+ * - Matrices are row-major; weights are stored [in, out] ("transposed" as on
+ *   the pages: W_lat [D,R], Wg/Wu [R,H], Wd [H,R], W2 [R,V]).
+ * - Alignment: every bf16 pointer must be 16-byte aligned and every leading
+ *   dimension (ld_*) a multiple of 8 elements, else XP_ERR_ALIGN.  Sizes are
+ *   otherwise free (V need not be a multiple of 8 for xp_add_argmax).
+ * - Workspace: an opaque caller-provided device buffer of at least the bytes
+ *   the matching *_workspace_size() returns, 256-byte aligned, ZEROED ONCE
+ *   (e.g. cudaMemsetAsync) before its first use.  Every call leaves its
+ *   reduction state zero again, so one workspace serves any number of calls,
+ *   but calls that share a workspace must not overlap on the GPU (use one
+ *   stream, or one workspace per stream).  A workspace sized for one entry
+ *   point may serve a smaller one: xp_jacobi_workspace_size() covers
+ *   xp_latent_pass and xp_readout_argmax/xp_add_argmax of the same shapes.
+ * - Errors: host-side checks run before any launch and return a status
+ *   without touching memory.  Device-side conditions (a token outside
+ *   [0, V)) are clamped, recorded in the workspace and reported by
+ *   xp_read_error(); kernels never trap.
+ * - blk must not alias any other argument.  Slot 0 of blk is never written.
+ */
+#ifndef XPRESS_H
+#define XPRESS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define XP_API __attribute__((visibility("default")))
+#else
+#define XP_API
+#endif
+
+typedef uint16_t xp_bf16;                 /* bfloat16 bit pattern */
+typedef struct CUstream_st* xp_stream_t;  /* the same type as cudaStream_t */
+
+typedef int32_t xp_status;
+#define XP_OK 0
+#define XP_ERR_NULL 1          /* a required pointer is NULL */
+#define XP_ERR_SHAPE 2         /* inconsistent or out-of-range sizes */
+#define XP_ERR_ALIGN 3         /* pointer or leading dimension misaligned */
+#define XP_ERR_WORKSPACE 4     /* workspace missing, too small or misaligned */
+#define XP_ERR_LAUNCH 5        /* a CUDA launch or driver call failed */
+#define XP_ERR_UNSUPPORTED 6   /* current device is not sm_103 (GB300) */
+
+/* Device-side error bits reported by xp_read_error(). */
+#define XP_DEVERR_TOKEN 1u     /* a token in blk/am1 was outside [0, V) and was clamped */
+#define XP_DEVERR_TIMEOUT 2u   /* a bounded device-side wait gave up */
+
+/* Human-readable name of a status code (static string, never NULL). */
+XP_API const char* xp_status_string(xp_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+XP_API int32_t xp_version(void);
+
+/* ------------------------------------------------------------------------
+ * xp_add_argmax -- the fused add + vocab-wide argmax, written into blk.
+ * Pages: fused_add_argmax_to_blk and its two kernels
+ * (_xpress_add_argmax_partial_kernel, _xpress_add_argmax_reduce_to_blk_kernel).
+ *
+ *   for r in [0, rows):  n = r / (B-1), j = r % (B-1)
+ *     blk[n*B + 1 + j] = min { v : s[r,v] = max_v' s[r,v'] },
+ *     s[r,v] = bf16_round_nearest_even(float(base[r*ld_base+v]) + float(bias[r*ld_bias+v]))
+ *
+ * -0 and +0 compare equal; ties go to the lowest v.  Inputs must be finite.
+ * d_base, d_bias: [rows, V] bf16 with row strides ld_base, ld_bias >= V.
+ * d_blk: [N, B] int64, rows == N*(B-1), B >= 2, N >= 0 (N == 0 is a no-op).
+ * V in [1, 2^31 - 1].  Workspace: xp_add_argmax_workspace_size(rows, V).
+ * ---------------------------------------------------------------------- */
+XP_API size_t xp_add_argmax_workspace_size(int64_t rows, int64_t V);
+XP_API xp_status xp_add_argmax(const xp_bf16* d_base, int64_t ld_base, const xp_bf16* d_bias,
+                        int64_t ld_bias, int64_t rows, int64_t V, int64_t* d_blk, int64_t N,
+                        int64_t B, void* d_workspace, size_t workspace_bytes, xp_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * xp_latent_pass -- the fused latent stage.
+ * Pages: xpress_latent_pass / _xpress_latent_kernel (in-kernel MLP form).
+ *
+ *   prev[n,0] = am1[n], prev[n,b] = blk[n,b-1]            (b >= 1)
+ *   x[n,b,:]  = float(hcache[n,b,:]) + E[prev[n,b],:] @ W_lat     (fp32 accumulate)
+ *   u[n,b,r]  = sum_{j<=b} L[b,j,r] * x[n,j,r]
+ *   ub = bf16(u);  g = ub @ Wg;  v = ub @ Wu;  m = bf16(g * sigmoid(g) * v)
+ *   lat_out[n,b-1,:] = bf16(u[n,b,:] + m @ Wd)           (b = 1..B-1)
+ *
+ * d_blk [N,B] int64, d_am1 [N] int64, d_hcache [N,B,R] bf16, d_E [V,D] bf16,
+ * d_W_lat [D,R] bf16, d_L [B,B,R] float32 (entries above the diagonal are
+ * ignored), d_Wg/d_Wu [R,H] bf16, d_Wd [H,R] bf16, d_lat_out [N,B-1,R] bf16.
+ * All dense (no padding).  Constraints: 2 <= B <= 16, R and D multiples of 64,
+ * H a multiple of 64.  Workspace: xp_latent_workspace_size(N,B,D,R,H).
+ * ---------------------------------------------------------------------- */
+XP_API size_t xp_latent_workspace_size(int64_t N, int64_t B, int64_t D, int64_t R, int64_t H);
+XP_API xp_status xp_latent_pass(const int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_hcache,
+                         const xp_bf16* d_E, const xp_bf16* d_W_lat, const float* d_L,
+                         const xp_bf16* d_Wg, const xp_bf16* d_Wu, const xp_bf16* d_Wd,
+                         xp_bf16* d_lat_out, int64_t N, int64_t B, int64_t V, int64_t D, int64_t R,
+                         int64_t H, void* d_workspace, size_t workspace_bytes, xp_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * xp_readout_argmax -- the readout matmul with the add + argmax fused into
+ * its epilogue (the caller's `lat_out @ W2` followed by fused_add_argmax_to_blk,
+ * without the bias or the logits ever reaching memory):
+ *
+ *   bias[r,v] = bf16(sum_k lat[r,k] * W2[k,v])              (fp32 accumulate)
+ *   s[r,v]    = bf16(float(base[r*ld_base+v]) + float(bias[r,v]))
+ *   blk[n*B + 1 + j] = lowest argmax_v s[r,v]               r = n*(B-1)+j
+ *
+ * d_lat [rows,R] bf16 dense, d_W2 [R,V] bf16 dense, d_base [rows,V] (ld_base).
+ * R a multiple of 64, V a multiple of 8.  d_changed (nullable, device int32):
+ * incremented by the number of slots whose token differs from the value blk
+ * held before the call.  Workspace: xp_readout_workspace_size(rows, V).
+ * ---------------------------------------------------------------------- */
+XP_API size_t xp_readout_workspace_size(int64_t rows, int64_t V);
+XP_API xp_status xp_readout_argmax(const xp_bf16* d_lat, const xp_bf16* d_W2, const xp_bf16* d_base,
+                            int64_t ld_base, int64_t rows, int64_t V, int64_t R, int64_t* d_blk,
+                            int64_t N, int64_t B, int32_t* d_changed, void* d_workspace,
+                            size_t workspace_bytes, xp_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * xp_jacobi_pass -- one whole pass: xp_latent_pass, then xp_readout_argmax on
+ * its output (kept in the workspace), writing blk[:,1:] in place.  Repeated
+ * calls iterate the Jacobi fixpoint: each pass reads the blk written by the
+ * previous one (_xpress_add_argmax_reduce_to_blk_kernel docstring).
+ * d_changed as in xp_readout_argmax.  Constraints: those of both stages.
+ * Workspace: xp_jacobi_workspace_size(N,B,V,D,R,H).
+ * ---------------------------------------------------------------------- */
+XP_API size_t xp_jacobi_workspace_size(int64_t N, int64_t B, int64_t V, int64_t D, int64_t R, int64_t H);
+XP_API xp_status xp_jacobi_pass(int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_hcache,
+                         const xp_bf16* d_E, const xp_bf16* d_W_lat, const float* d_L,
+                         const xp_bf16* d_Wg, const xp_bf16* d_Wu, const xp_bf16* d_Wd,
+                         const xp_bf16* d_W2, const xp_bf16* d_base, int64_t ld_base, int64_t N,
+                         int64_t B, int64_t V, int64_t D, int64_t R, int64_t H,
+                         int32_t* d_changed, void* d_workspace, size_t workspace_bytes,
+                         xp_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * xp_read_error -- copy the workspace's device-side error bits (XP_DEVERR_*)
+ * to *host_bits and clear them.  Synchronises `stream`; do not call it while
+ * the stream is being captured into a CUDA graph.
+ * ---------------------------------------------------------------------- */
+XP_API xp_status xp_read_error(void* d_workspace, xp_stream_t stream, uint32_t* host_bits);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* XPRESS_H */

@@ -1,0 +1,139 @@
+// xp_add_argmax.cu -- the fused add + vocab-wide argmax written into blk.
+//
+// Method (vLLM docs, vllm.v1.worker.gpu.spec_decode.xpress.kernels,
+// fused_add_argmax_to_blk with _xpress_add_argmax_partial_kernel and
+// _xpress_add_argmax_reduce_to_blk_kernel): for row r = n*(B-1)+j,
+// blk[n, 1+j] = lowest v maximising bf16(base[r,v] + bias[r,v]).
+//
+// GB300 design: one launch, HBM-bound streaming.  Each CTA owns one
+// (row, CHUNK-wide vocab slice); every thread issues all of its 16-byte loads
+// of base and bias up front (VEC vectors of 8 elements each, coalesced per
+// vector step), adds them as packed bf16 pairs (one rounding, RNE) and keeps a
+// packed running maximum.  The CTA reduces the maximum, the threads that hold
+// it search their registers for its first position, and the CTA folds the
+// (value, lowest index) pair into the row's 64-bit key with atomicMax.  The
+// last CTA of a row (arrival counter) writes blk and re-zeroes the key and
+// counter, so the workspace is clean for the next call and no second launch
+// or partial buffer is needed.
+#include "xp_common.cuh"
+#include "xp_internal.h"
+
+namespace xp {
+
+template <int THREADS, int VEC>
+__global__ void __launch_bounds__(THREADS)
+add_argmax_kernel(const uint16_t* __restrict__ base, int64_t ld_base, const uint16_t* __restrict__ bias,
+                  int64_t ld_bias, int32_t V, int32_t nchunks, int64_t* __restrict__ blk, int32_t B,
+                  unsigned long long* __restrict__ keys, unsigned int* __restrict__ cnt) {
+  constexpr int CHUNK = THREADS * VEC * 8;
+  constexpr int WARPS = THREADS / 32;
+  __shared__ float s_max[WARPS];
+  __shared__ int s_idx[WARPS];
+
+  const int t = threadIdx.x;
+  const int64_t unit = blockIdx.x;
+  const int64_t row = unit / nchunks;
+  const int32_t chunk = (int32_t)(unit - row * nchunks);
+  const uint16_t* pa = base + row * ld_base;
+  const uint16_t* pb = bias + row * ld_bias;
+  const int32_t v0 = chunk * CHUNK;
+
+  // s[j][k]: packed sums of elements v0 + (j*THREADS + t)*8 + 2k, +1.
+  uint32_t s[VEC][4];
+  uint4 a[VEC], b[VEC];
+#pragma unroll
+  for (int j = 0; j < VEC; ++j) {
+    const int32_t v = v0 + (j * THREADS + t) * 8;
+    if (v + 8 <= V) {
+      a[j] = ld_stream_v4(pa + v);
+      b[j] = ld_stream_v4(pb + v);
+    } else {
+      // ragged tail: element-wise, padding with -inf (never selected: the
+      // search below only accepts indices < V)
+      uint32_t wa[4], wb[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t lo_a = 0xff80u, hi_a = 0xff80u, lo_b = 0u, hi_b = 0u;
+        if (v + 2 * k < V) { lo_a = pa[v + 2 * k]; lo_b = pb[v + 2 * k]; }
+        if (v + 2 * k + 1 < V) { hi_a = pa[v + 2 * k + 1]; hi_b = pb[v + 2 * k + 1]; }
+        wa[k] = lo_a | (hi_a << 16);
+        wb[k] = lo_b | (hi_b << 16);
+      }
+      a[j] = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+      b[j] = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+    }
+  }
+  uint32_t m2 = 0xff80ff80u;  // (-inf, -inf)
+#pragma unroll
+  for (int j = 0; j < VEC; ++j) {
+    s[j][0] = bf16x2_add(a[j].x, b[j].x);
+    s[j][1] = bf16x2_add(a[j].y, b[j].y);
+    s[j][2] = bf16x2_add(a[j].z, b[j].z);
+    s[j][3] = bf16x2_add(a[j].w, b[j].w);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m2 = bf16x2_max(m2, s[j][k]);
+  }
+  const float mt = fmaxf(bf16lo_to_f32(m2), bf16hi_to_f32(m2));
+
+  // CTA maximum
+  float m = mt;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((t & 31) == 0) s_max[t >> 5] = m;
+  __syncthreads();
+  float mc = s_max[0];
+#pragma unroll
+  for (int w = 1; w < WARPS; ++w) mc = fmaxf(mc, s_max[w]);
+
+  // first position of the CTA maximum among this thread's elements
+  // (positions increase with j, then k, then the half)
+  int cand = 0x7fffffff;
+  if (mt == mc) {
+#pragma unroll
+    for (int j = VEC - 1; j >= 0; --j) {
+#pragma unroll
+      for (int k = 3; k >= 0; --k) {
+        const int32_t v = v0 + (j * THREADS + t) * 8 + 2 * k;
+        if (bf16hi_to_f32(s[j][k]) == mc && v + 1 < V) cand = v + 1;
+        if (bf16lo_to_f32(s[j][k]) == mc && v < V) cand = v;
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+  if ((t & 31) == 0) s_idx[t >> 5] = cand;
+  __syncthreads();
+  if (t == 0) {
+    int ic = s_idx[0];
+#pragma unroll
+    for (int w = 1; w < WARPS; ++w) ic = min(ic, s_idx[w]);
+    atomicMax(&keys[row], make_key(mc, (uint32_t)ic));
+    __threadfence();
+    const unsigned int arrived = atomicAdd(&cnt[row], 1u);
+    if (arrived == (unsigned int)nchunks - 1u) {
+      __threadfence();
+      const unsigned long long k = atomicExch(&keys[row], 0ull);
+      cnt[row] = 0u;
+      const int64_t n = row / (B - 1), jj = row - n * (B - 1);
+      blk[n * B + 1 + jj] = (int64_t)key_index(k);
+    }
+  }
+}
+
+constexpr int AA_THREADS = 256;
+constexpr int AA_VEC = 4;
+
+xp_status launch_add_argmax(const uint16_t* base, int64_t ld_base, const uint16_t* bias, int64_t ld_bias,
+                            int64_t rows, int64_t V, int64_t* blk, int64_t B, void* ws,
+                            cudaStream_t stream) {
+  ArgmaxWs w = argmax_ws(ws, rows);
+  if (rows <= 0) return XP_OK;
+  constexpr int CHUNK = AA_THREADS * AA_VEC * 8;
+  const int64_t nchunks = (V + CHUNK - 1) / CHUNK;
+  const int64_t grid = rows * nchunks;
+  add_argmax_kernel<AA_THREADS, AA_VEC><<<(unsigned int)grid, AA_THREADS, 0, stream>>>(
+      base, ld_base, bias, ld_bias, (int32_t)V, (int32_t)nchunks, blk, (int32_t)B, w.keys, w.cnt);
+  return cudaGetLastError() == cudaSuccess ? XP_OK : XP_ERR_LAUNCH;
+}
+
+}  // namespace xp

@@ -1,0 +1,125 @@
+// xp_capi.cu -- the extern "C" entry points of libxpress.so: argument
+// validation (before any launch), workspace checks, and dispatch to the
+// launchers.  See include/xpress.h for the contract of each call.
+#include <stdint.h>
+
+#include "xp_common.cuh"
+#include "xp_internal.h"
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+bool aligned256(const void* p) { return ((uintptr_t)p & 255u) == 0; }
+
+// The kernels are compiled for sm_103a only; refuse other devices up front
+// rather than failing at launch.
+xp_status check_device() {
+  static int cached[64];  // 0 unknown, 1 ok, 2 unsupported
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return XP_ERR_LAUNCH;
+  if (dev < 0 || dev >= 64) return XP_ERR_UNSUPPORTED;
+  if (cached[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return XP_ERR_LAUNCH;
+    cached[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  return cached[dev] == 1 ? XP_OK : XP_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* xp_status_string(xp_status s) {
+  switch (s) {
+    case XP_OK: return "XP_OK";
+    case XP_ERR_NULL: return "XP_ERR_NULL: a required pointer is NULL";
+    case XP_ERR_SHAPE: return "XP_ERR_SHAPE: inconsistent or out-of-range sizes";
+    case XP_ERR_ALIGN: return "XP_ERR_ALIGN: pointer or leading dimension misaligned";
+    case XP_ERR_WORKSPACE: return "XP_ERR_WORKSPACE: workspace missing, too small or misaligned";
+    case XP_ERR_LAUNCH: return "XP_ERR_LAUNCH: a CUDA launch or driver call failed";
+    case XP_ERR_UNSUPPORTED: return "XP_ERR_UNSUPPORTED: the current device is not sm_103 (GB300)";
+    default: return "unknown xp_status";
+  }
+}
+
+int32_t xp_version(void) { return 100; }
+
+size_t xp_add_argmax_workspace_size(int64_t rows, int64_t V) {
+  (void)V;
+  if (rows < 0) return 0;
+  return xp::argmax_ws_bytes(rows);
+}
+
+xp_status xp_add_argmax(const xp_bf16* d_base, int64_t ld_base, const xp_bf16* d_bias, int64_t ld_bias,
+                        int64_t rows, int64_t V, int64_t* d_blk, int64_t N, int64_t B, void* d_workspace,
+                        size_t workspace_bytes, xp_stream_t stream) {
+  if (N < 0 || B < 2 || V < 1 || V > (int64_t(1) << 30) || rows != N * (B - 1)) return XP_ERR_SHAPE;
+  if (ld_base < V || ld_bias < V) return XP_ERR_SHAPE;
+  if (rows == 0) return XP_OK;
+  if (!d_base || !d_bias || !d_blk || !d_workspace) return XP_ERR_NULL;
+  if (!aligned16(d_base) || !aligned16(d_bias) || (ld_base & 7) || (ld_bias & 7) || ((uintptr_t)d_blk & 7))
+    return XP_ERR_ALIGN;
+  if (!aligned256(d_workspace) || workspace_bytes < xp::argmax_ws_bytes(rows)) return XP_ERR_WORKSPACE;
+  xp_status st = check_device();
+  if (st != XP_OK) return st;
+  return xp::launch_add_argmax(d_base, ld_base, d_bias, ld_bias, rows, V, d_blk, B, d_workspace,
+                               (cudaStream_t)stream);
+}
+
+size_t xp_readout_workspace_size(int64_t rows, int64_t V) {
+  (void)V;
+  if (rows < 0) return 0;
+  return xp::argmax_ws_bytes(rows);
+}
+
+xp_status xp_readout_argmax(const xp_bf16* d_lat, const xp_bf16* d_W2, const xp_bf16* d_base, int64_t ld_base,
+                            int64_t rows, int64_t V, int64_t R, int64_t* d_blk, int64_t N, int64_t B,
+                            int32_t* d_changed, void* d_workspace, size_t workspace_bytes, xp_stream_t stream) {
+  if (N < 0 || B < 2 || V < 1 || V > (int64_t(1) << 30) || rows != N * (B - 1)) return XP_ERR_SHAPE;
+  if (R < 8 || R > 512 || ld_base < V || rows > (int64_t(1) << 24)) return XP_ERR_SHAPE;
+  if (rows == 0) return XP_OK;
+  if (!d_lat || !d_W2 || !d_base || !d_blk || !d_workspace) return XP_ERR_NULL;
+  if (!aligned16(d_lat) || !aligned16(d_W2) || !aligned16(d_base) || (ld_base & 7) || (V & 7) || (R & 7) ||
+      ((uintptr_t)d_blk & 7) || ((uintptr_t)d_changed & 3))
+    return XP_ERR_ALIGN;
+  if (!aligned256(d_workspace) || workspace_bytes < xp::argmax_ws_bytes(rows)) return XP_ERR_WORKSPACE;
+  xp_status st = check_device();
+  if (st != XP_OK) return st;
+  return xp::launch_readout_argmax(d_lat, d_W2, d_base, ld_base, rows, V, R, d_blk, B, d_changed, d_workspace,
+                                   (cudaStream_t)stream);
+}
+
+xp_status xp_read_error(void* d_workspace, xp_stream_t stream, uint32_t* host_bits) {
+  if (!d_workspace || !host_bits) return XP_ERR_NULL;
+  if (!aligned256(d_workspace)) return XP_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  unsigned int bits = 0;
+  if (cudaMemcpyAsync(&bits, d_workspace, sizeof(bits), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return XP_ERR_LAUNCH;
+  if (cudaMemsetAsync(d_workspace, 0, sizeof(bits), s) != cudaSuccess) return XP_ERR_LAUNCH;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return XP_ERR_LAUNCH;
+  *host_bits = bits;
+  return XP_OK;
+}
+
+}  // extern "C"
+
+// ---- stages not yet wired (temporary) ----
+extern "C" {
+size_t xp_latent_workspace_size(int64_t, int64_t, int64_t, int64_t, int64_t) { return 256; }
+xp_status xp_latent_pass(const int64_t*, const int64_t*, const xp_bf16*, const xp_bf16*, const xp_bf16*,
+                         const float*, const xp_bf16*, const xp_bf16*, const xp_bf16*, xp_bf16*, int64_t,
+                         int64_t, int64_t, int64_t, int64_t, int64_t, void*, size_t, xp_stream_t) {
+  return XP_ERR_UNSUPPORTED;
+}
+size_t xp_jacobi_workspace_size(int64_t, int64_t, int64_t, int64_t, int64_t, int64_t) { return 256; }
+xp_status xp_jacobi_pass(int64_t*, const int64_t*, const xp_bf16*, const xp_bf16*, const xp_bf16*, const float*,
+                         const xp_bf16*, const xp_bf16*, const xp_bf16*, const xp_bf16*, const xp_bf16*, int64_t,
+                         int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int32_t*, void*, size_t,
+                         xp_stream_t) {
+  return XP_ERR_UNSUPPORTED;
+}
+}

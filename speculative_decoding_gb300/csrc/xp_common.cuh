@@ -1,0 +1,109 @@
+// xp_common.cuh -- small device helpers shared by the xpress kernels:
+// packed bf16 arithmetic, the order-preserving (value, lowest index) key used
+// to fold partial argmaxes across CTAs, and the workspace layout.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/xpress.h"
+
+namespace xp {
+
+// ---------------------------------------------------------------------------
+// packed bf16 arithmetic (two values per 32-bit word; the lower address is the
+// low half)
+// ---------------------------------------------------------------------------
+
+// Correctly rounded (round-to-nearest-even) bf16 sum of two packed pairs.
+// A single rounding of the exact sum equals rounding the fp32 sum, which is
+// the rounding the method prescribes (the sum is cast back to bf16 before the
+// compare).
+__device__ __forceinline__ uint32_t bf16x2_add(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Lane-wise maximum of two packed pairs (inputs are finite).
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Two fp32 values -> packed bf16 pair, each rounded to nearest even
+// (lo goes to the low half).
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// ---------------------------------------------------------------------------
+// (value, index) keys: a 64-bit unsigned integer whose order is "larger value
+// first, then lower index", so atomicMax over keys folds partial argmaxes with
+// the lowest-index tie rule in any arrival order.  -0 is mapped to +0 first
+// so the two zeros tie.  Key 0 is below every real key (the empty state).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long make_key(float val, uint32_t idx) {
+  uint32_t b = __float_as_uint(val);
+  if (b == 0x80000000u) b = 0u;
+  uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((unsigned long long)ord << 32) | (unsigned long long)(0xffffffffu - idx);
+}
+__device__ __forceinline__ uint32_t key_index(unsigned long long k) {
+  return 0xffffffffu - (uint32_t)(k & 0xffffffffull);
+}
+
+// ---------------------------------------------------------------------------
+// streaming loads
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// workspace layout (all offsets 256-byte aligned)
+//   [0, 256)            header: error bits, grid-done counters
+//   keys  u64[rows]     per-row folded (value, index) key, zero between calls
+//   cnt   u32[rows]     per-row arrival counter, zero between calls
+//   then the latent stage's buffers (see xp_latent.cu)
+// ---------------------------------------------------------------------------
+struct WsHeader {
+  unsigned int err;         // XP_DEVERR_* bits
+  unsigned int done;        // CTAs of the current readout grid that finished
+  unsigned int pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct ArgmaxWs {
+  WsHeader* hdr;
+  unsigned long long* keys;
+  unsigned int* cnt;
+};
+
+__host__ inline size_t argmax_ws_bytes(int64_t rows) {
+  return 256 + align256(sizeof(unsigned long long) * (size_t)rows) + align256(4 * (size_t)rows);
+}
+__host__ inline ArgmaxWs argmax_ws(void* ws, int64_t rows) {
+  char* p = (char*)ws;
+  ArgmaxWs w;
+  w.hdr = (WsHeader*)p;
+  w.keys = (unsigned long long*)(p + 256);
+  w.cnt = (unsigned int*)(p + 256 + align256(sizeof(unsigned long long) * (size_t)rows));
+  return w;
+}
+
+__device__ __forceinline__ void flag_error(WsHeader* h, unsigned int bits) { atomicOr(&h->err, bits); }
+
+}  // namespace xp

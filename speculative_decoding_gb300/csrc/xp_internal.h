@@ -1,0 +1,19 @@
+// xp_internal.h -- launchers behind the C ABI (host side, not exported).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/xpress.h"
+
+namespace xp {
+
+xp_status launch_add_argmax(const uint16_t* base, int64_t ld_base, const uint16_t* bias, int64_t ld_bias,
+                            int64_t rows, int64_t V, int64_t* blk, int64_t B, void* ws,
+                            cudaStream_t stream);
+
+xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2, const uint16_t* base, int64_t ld_base,
+                                int64_t rows, int64_t V, int64_t R, int64_t* blk, int64_t B, int32_t* changed,
+                                void* ws, cudaStream_t stream);
+
+}  // namespace xp

@@ -1,0 +1,63 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol
+include/xpress.h declares, and rejects bad arguments on the host before any
+CUDA call (so these checks run on a CPU-only machine)."""
+
+import ctypes
+
+import pytest
+
+from speculative_decoding_gb300 import build, xpress
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return xpress.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = xpress.declared_symbols()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(xpress._SIGS), "binding signatures cover exactly the header"
+
+
+def test_status_strings(L):
+    for st in range(7):
+        assert xpress.status_string(st).startswith("XP_")
+    assert "unknown" in xpress.status_string(99)
+    assert L.xp_version() >= 100
+
+
+def test_workspace_sizes_monotone(L):
+    a = xpress.add_argmax_workspace_size(480, 152064)
+    assert a >= 256 + 480 * 12 and a % 256 == 0
+    assert xpress.add_argmax_workspace_size(960, 152064) > a
+
+
+FAKE = 1 << 20   # a non-null, 256-aligned dummy address; never dereferenced
+
+
+def _aa(rows=6, V=1000, N=2, B=4, ld=1000, base=FAKE, bias=FAKE, blk=FAKE, ws=FAKE, nbytes=1 << 20):
+    return xpress.lib().xp_add_argmax(base, ld, bias, ld, rows, V, blk, N, B, ws, nbytes, None)
+
+
+def test_add_argmax_host_validation(L):
+    assert _aa(rows=5) == xpress.XP_ERR_SHAPE                 # rows != N*(B-1)
+    assert _aa(B=1, rows=0) == xpress.XP_ERR_SHAPE
+    assert _aa(V=0) == xpress.XP_ERR_SHAPE
+    assert _aa(ld=999) == xpress.XP_ERR_SHAPE                 # ld < V
+    assert _aa(N=0, rows=0) == xpress.XP_OK                   # empty: no-op
+    assert _aa(base=0) == xpress.XP_ERR_NULL
+    assert _aa(ws=0) == xpress.XP_ERR_NULL
+    assert _aa(base=FAKE + 8) == xpress.XP_ERR_ALIGN
+    assert _aa(ld=1004) == xpress.XP_ERR_ALIGN
+    assert _aa(ws=FAKE + 16) == xpress.XP_ERR_WORKSPACE
+    assert _aa(nbytes=64) == xpress.XP_ERR_WORKSPACE
+
+
+def test_read_error_validation(L):
+    bits = ctypes.c_uint32()
+    assert L.xp_read_error(None, None, ctypes.byref(bits)) == xpress.XP_ERR_NULL
+    assert L.xp_read_error(FAKE + 1, None, ctypes.byref(bits)) == xpress.XP_ERR_WORKSPACE
