@@ -92,6 +92,82 @@ xp_status xp_readout_argmax(const xp_bf16* d_lat, const xp_bf16* d_W2, const xp_
                                    (cudaStream_t)stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Shape and alignment checks shared by the latent stage and the full pass.
+xp_status check_latent_args(const int64_t* blk, const int64_t* am1, const xp_bf16* hcache, const xp_bf16* E,
+                            const xp_bf16* W_lat, const float* L, const xp_bf16* Wg, const xp_bf16* Wu,
+                            const xp_bf16* Wd, int64_t N, int64_t B, int64_t V, int64_t D, int64_t R, int64_t H) {
+  if (N < 0 || B < 2 || B > 16 || V < 1 || V > (int64_t(1) << 30)) return XP_ERR_SHAPE;
+  if (D < 8 || D > (int64_t(1) << 20) || R < 16 || R > 512 || H < 64 || H > (int64_t(1) << 16)) return XP_ERR_SHAPE;
+  if (N * B > (int64_t(1) << 22)) return XP_ERR_SHAPE;
+  if (N == 0) return XP_OK;
+  if (!blk || !am1 || !hcache || !E || !W_lat || !L || !Wg || !Wu || !Wd) return XP_ERR_NULL;
+  if ((D & 7) || (R & 15) || (H & 63)) return XP_ERR_ALIGN;
+  if (!aligned16(hcache) || !aligned16(E) || !aligned16(W_lat) || !aligned16(Wg) || !aligned16(Wu) ||
+      !aligned16(Wd) || ((uintptr_t)L & 3) || ((uintptr_t)blk & 7) || ((uintptr_t)am1 & 7))
+    return XP_ERR_ALIGN;
+  return XP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t xp_latent_workspace_size(int64_t N, int64_t B, int64_t D, int64_t R, int64_t H) {
+  (void)D;
+  if (N < 0 || B < 2 || R < 0 || H < 0) return 0;
+  return xp::latent_ws_layout(N, B, R, H).total_latent;
+}
+
+xp_status xp_latent_pass(const int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_hcache, const xp_bf16* d_E,
+                         const xp_bf16* d_W_lat, const float* d_L, const xp_bf16* d_Wg, const xp_bf16* d_Wu,
+                         const xp_bf16* d_Wd, xp_bf16* d_lat_out, int64_t N, int64_t B, int64_t V, int64_t D,
+                         int64_t R, int64_t H, void* d_workspace, size_t workspace_bytes, xp_stream_t stream) {
+  xp_status st = check_latent_args(d_blk, d_am1, d_hcache, d_E, d_W_lat, d_L, d_Wg, d_Wu, d_Wd, N, B, V, D, R, H);
+  if (st != XP_OK || N == 0) return st;
+  if (!d_lat_out || !d_workspace) return XP_ERR_NULL;
+  if (!aligned16(d_lat_out)) return XP_ERR_ALIGN;
+  if (!aligned256(d_workspace) || workspace_bytes < xp::latent_ws_layout(N, B, R, H).total_latent)
+    return XP_ERR_WORKSPACE;
+  st = check_device();
+  if (st != XP_OK) return st;
+  return xp::launch_latent(d_blk, d_am1, d_hcache, d_E, d_W_lat, d_L, d_Wg, d_Wu, d_Wd, d_lat_out, N, B, V, D, R, H,
+                           d_workspace, (cudaStream_t)stream);
+}
+
+size_t xp_jacobi_workspace_size(int64_t N, int64_t B, int64_t V, int64_t D, int64_t R, int64_t H) {
+  (void)V;
+  (void)D;
+  if (N < 0 || B < 2 || R < 0 || H < 0) return 0;
+  return xp::latent_ws_layout(N, B, R, H).total_pass;
+}
+
+xp_status xp_jacobi_pass(int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_hcache, const xp_bf16* d_E,
+                         const xp_bf16* d_W_lat, const float* d_L, const xp_bf16* d_Wg, const xp_bf16* d_Wu,
+                         const xp_bf16* d_Wd, const xp_bf16* d_W2, const xp_bf16* d_base, int64_t ld_base, int64_t N,
+                         int64_t B, int64_t V, int64_t D, int64_t R, int64_t H, int32_t* d_changed,
+                         void* d_workspace, size_t workspace_bytes, xp_stream_t stream) {
+  xp_status st = check_latent_args(d_blk, d_am1, d_hcache, d_E, d_W_lat, d_L, d_Wg, d_Wu, d_Wd, N, B, V, D, R, H);
+  if (st != XP_OK || N == 0) return st;
+  if (ld_base < V) return XP_ERR_SHAPE;
+  if (!d_W2 || !d_base || !d_workspace) return XP_ERR_NULL;
+  if (!aligned16(d_W2) || !aligned16(d_base) || (ld_base & 7) || (V & 7) || ((uintptr_t)d_changed & 3))
+    return XP_ERR_ALIGN;
+  const xp::LatentWsLayout lay = xp::latent_ws_layout(N, B, R, H);
+  if (!aligned256(d_workspace) || workspace_bytes < lay.total_pass) return XP_ERR_WORKSPACE;
+  st = check_device();
+  if (st != XP_OK) return st;
+  uint16_t* lat = reinterpret_cast<uint16_t*>(static_cast<char*>(d_workspace) + lay.lat);
+  st = xp::launch_latent(d_blk, d_am1, d_hcache, d_E, d_W_lat, d_L, d_Wg, d_Wu, d_Wd, lat, N, B, V, D, R, H,
+                         d_workspace, (cudaStream_t)stream);
+  if (st != XP_OK) return st;
+  return xp::launch_readout_argmax(lat, d_W2, d_base, ld_base, N * (B - 1), V, R, d_blk, B, d_changed, d_workspace,
+                                   (cudaStream_t)stream);
+}
+
 xp_status xp_read_error(void* d_workspace, xp_stream_t stream, uint32_t* host_bits) {
   if (!d_workspace || !host_bits) return XP_ERR_NULL;
   if (!aligned256(d_workspace)) return XP_ERR_WORKSPACE;
@@ -106,20 +182,3 @@ xp_status xp_read_error(void* d_workspace, xp_stream_t stream, uint32_t* host_bi
 }
 
 }  // extern "C"
-
-// ---- stages not yet wired (temporary) ----
-extern "C" {
-size_t xp_latent_workspace_size(int64_t, int64_t, int64_t, int64_t, int64_t) { return 256; }
-xp_status xp_latent_pass(const int64_t*, const int64_t*, const xp_bf16*, const xp_bf16*, const xp_bf16*,
-                         const float*, const xp_bf16*, const xp_bf16*, const xp_bf16*, xp_bf16*, int64_t,
-                         int64_t, int64_t, int64_t, int64_t, int64_t, void*, size_t, xp_stream_t) {
-  return XP_ERR_UNSUPPORTED;
-}
-size_t xp_jacobi_workspace_size(int64_t, int64_t, int64_t, int64_t, int64_t, int64_t) { return 256; }
-xp_status xp_jacobi_pass(int64_t*, const int64_t*, const xp_bf16*, const xp_bf16*, const xp_bf16*, const float*,
-                         const xp_bf16*, const xp_bf16*, const xp_bf16*, const xp_bf16*, const xp_bf16*, int64_t,
-                         int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int32_t*, void*, size_t,
-                         xp_stream_t) {
-  return XP_ERR_UNSUPPORTED;
-}
-}

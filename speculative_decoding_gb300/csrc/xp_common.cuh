@@ -104,6 +104,30 @@ __host__ inline ArgmaxWs argmax_ws(void* ws, int64_t rows) {
   return w;
 }
 
+// Latent / full-pass workspace: the argmax part for rows = N*(B-1), then
+//   u   fp32 [N*B, R]   mixer output (the MLP residual)
+//   ub  bf16 [N*B, R]   bf16(u), the MLP input
+//   m   bf16 [N*B, H]   bf16(silu(ub@Wg) * (ub@Wu))
+//   lat bf16 [N*(B-1), R]  the latent read by the readout (full pass only)
+struct LatentWsLayout {
+  size_t u, ub, m, lat, total_latent, total_pass;
+};
+__host__ inline LatentWsLayout latent_ws_layout(int64_t N, int64_t B, int64_t R, int64_t H) {
+  LatentWsLayout L;
+  size_t off = argmax_ws_bytes(N * (B - 1));
+  L.u = off;
+  off += align256(4 * (size_t)(N * B * R));
+  L.ub = off;
+  off += align256(2 * (size_t)(N * B * R));
+  L.m = off;
+  off += align256(2 * (size_t)(N * B * H));
+  L.total_latent = off;
+  L.lat = off;
+  off += align256(2 * (size_t)(N * (B - 1) * R));
+  L.total_pass = off;
+  return L;
+}
+
 __device__ __forceinline__ void flag_error(WsHeader* h, unsigned int bits) { atomicOr(&h->err, bits); }
 
 }  // namespace xp

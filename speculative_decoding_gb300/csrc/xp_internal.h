@@ -16,4 +16,9 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2, const u
                                 int64_t rows, int64_t V, int64_t R, int64_t* blk, int64_t B, int32_t* changed,
                                 void* ws, cudaStream_t stream);
 
+xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* hcache, const uint16_t* E,
+                        const uint16_t* W_lat, const float* L, const uint16_t* Wg, const uint16_t* Wu,
+                        const uint16_t* Wd, uint16_t* lat_out, int64_t N, int64_t B, int64_t V, int64_t D, int64_t R,
+                        int64_t H, void* ws, cudaStream_t stream);
+
 }  // namespace xp

@@ -9,20 +9,23 @@
 // _xpress_add_argmax_partial_kernel).  The [rows, V] bias and logits never
 // reach memory.
 //
-// GB300 design (tcgen05 + TMA):
+// GB300 design (tcgen05 + TMEM + TMA):
 //   * one CTA per SM; CTA (m, j) owns M tile m (128 draft rows) and a
-//     contiguous range of 256-wide vocab tiles;
-//   * warp 0 (one thread) loads the CTA's 128 x R slice of lat ONCE into
-//     shared memory (it stays resident) and then streams W2 in 64 x 256
-//     K-chunks through a ring of stages, all with TMA (128-byte swizzle);
-//   * warp 1 (one thread) issues tcgen05.mma M=128 N=256 K=16 (bf16 in, fp32
-//     accumulate) into one of two 256-column TMEM accumulators, so the
-//     epilogue of tile t overlaps the MMAs of tile t+1;
+//     contiguous range of 128-wide vocab tiles;
+//   * the CTA's 128 x R slice of the latent (the MMA's A operand) is written
+//     ONCE into tensor memory (256 columns for R = 512) and every MMA reads
+//     it from there, which leaves shared memory to the streamed operands;
+//   * warp 0 (one thread) streams W2 in 64 x 128 K-chunks through a ring of
+//     stages and the matching 128 x 128 base tile into a second ring, all
+//     with TMA and 128-byte swizzle;
+//   * warp 1 (one thread) issues tcgen05.mma M=128 N=128 K=16 (A in TMEM,
+//     B in shared memory, fp32 accumulate) into one of two 128-column TMEM
+//     accumulators, so the epilogue of tile t overlaps the MMAs of tile t+1;
 //   * warps 2..9 drain the accumulator with tcgen05.ld (thread = one row,
-//     warp = a 32-lane quadrant and a 128-column half), round to bf16, add
-//     the base logits (prefetched one tile ahead into registers), and keep a
-//     running (max, first column) per row across the CTA's tiles (tiles and
-//     columns ascend, so a strict '>' keeps the lowest index);
+//     warp = a 32-lane quadrant and a 64-column half), round to bf16, add the
+//     base tile from shared memory and keep a running (max, first column)
+//     per row across the CTA's tiles (tiles and columns ascend, so a strict
+//     '>' keeps the lowest index);
 //   * each row's per-CTA winner is folded into a 64-bit (value, lowest
 //     index) key with atomicMax; the last CTA to finish writes blk, counts the
 //     changed slots and re-zeroes the keys.
@@ -34,19 +37,30 @@
 namespace xp {
 
 constexpr int RO_BM = 128;
-constexpr int RO_BN = 256;
+constexpr int RO_BN = 128;
 constexpr int RO_BK = 64;
 constexpr int RO_EPI_WARPS = 8;
-constexpr int RO_THREADS = (2 + RO_EPI_WARPS) * 32;
-constexpr uint32_t RO_A_CHUNK = RO_BM * RO_BK * 2;    // 16 KB per 64-wide K chunk
-constexpr uint32_t RO_B_STAGE = RO_BK * RO_BN * 2;    // 32 KB per stage
-constexpr uint32_t RO_B_BOX = RO_BK * 64 * 2;         // one 64 x 64 TMA box, 8 KB
-constexpr int RO_MAX_KCH = 8;                         // R <= 512
+// warp 0: W2 producer (left 64 columns of each stage); warp 1: MMA issuer;
+// warps 2..9: epilogue; warp 10: W2 producer (right 64 columns); warp 11:
+// base producer.  Several issuing threads keep more TMA transfers moving
+// than a single one can.
+constexpr int RO_WARP_W2B = 2 + RO_EPI_WARPS;
+constexpr int RO_WARP_BASE = RO_WARP_W2B + 1;
+constexpr int RO_THREADS = (RO_WARP_BASE + 1) * 32;
+constexpr uint32_t RO_BOX = 64 * 64 * 2;               // one 64 x 64 bf16 box (8 KB)
+constexpr uint32_t RO_B_STAGE = RO_BK * RO_BN * 2;     // W2 stage: 64 K x 128 N (16 KB)
+constexpr uint32_t RO_BASE_BOX = RO_BM * 64 * 2;       // base box: 128 rows x 64 cols (16 KB)
+constexpr uint32_t RO_BASE_TILE = RO_BM * RO_BN * 2;   // 32 KB
+constexpr int RO_NBASE = 2;
+constexpr int RO_MAX_KCH = 8;                          // R <= 512
+constexpr uint32_t RO_TMEM_A = 0;                      // A: columns [0, 32*kch)
+constexpr uint32_t RO_TMEM_ACC = 256;                  // accumulators: [256, 384), [384, 512)
 
 struct ReadoutParams {
-  const uint16_t* base;
-  int64_t ld_base;
-  int32_t rows, V, kch, mt, nt, per, stages, B;
+  const uint16_t* lat;
+  int32_t rows, V, R, kch, mt, nt, per, stages, B;
+  int32_t cs;       // CTAs per cluster: M tiles that share each W2 stage by multicast
+  int32_t mgroups;  // clusters along M (ceil(mt / cs))
   int64_t* blk;
   int32_t* changed;
   unsigned long long* keys;
@@ -55,21 +69,15 @@ struct ReadoutParams {
 
 // One 32-column chunk of one row: acc (fp32) -> bias = bf16(acc);
 // s = bf16(base + bias); update the running (best, first column).
-__device__ __forceinline__ void ro_chunk(const uint32_t (&r)[32], const uint4 (&bw)[4], int col0, int V,
+__device__ __forceinline__ void ro_chunk(const uint32_t (&r)[32], const uint32_t (&bw)[16], int col0, int V,
                                          bool all_valid, float& best, int& bidx) {
   uint32_t s2[16];
   uint32_t m2 = 0xff80ff80u;
 #pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    const uint32_t w[4] = {bw[v].x, bw[v].y, bw[v].z, bw[v].w};
-    const bool ok = all_valid || (col0 + 8 * v < V);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int q = 4 * v + k;
-      const uint32_t bias2 = f32x2_to_bf16x2(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]));
-      s2[q] = bf16x2_add(w[k], bias2);
-      if (ok) m2 = bf16x2_max(m2, s2[q]);
-    }
+  for (int q = 0; q < 16; ++q) {
+    const uint32_t bias2 = f32x2_to_bf16x2(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]));
+    s2[q] = bf16x2_add(bw[q], bias2);
+    if (all_valid || col0 + 2 * q < V) m2 = bf16x2_max(m2, s2[q]);
   }
   const float m = fmaxf(bf16lo_to_f32(m2), bf16hi_to_f32(m2));
   if (m > best || bidx < 0) {
@@ -87,51 +95,51 @@ __device__ __forceinline__ void ro_chunk(const uint32_t (&r)[32], const uint4 (&
   }
 }
 
-// base[row, n0 .. n0+127] -> 16 x 16 bytes (vectors past V are not read)
-__device__ __forceinline__ void ro_load_base(uint4 (&dst)[16], const uint16_t* brow, int n0, int V, bool row_ok) {
-#pragma unroll
-  for (int v = 0; v < 16; ++v) {
-    if (row_ok && n0 + 8 * v < V)
-      dst[v] = ld_stream_v4(brow + n0 + 8 * v);
-    else
-      dst[v] = make_uint4(0, 0, 0, 0);
-  }
-}
-
 __global__ void __launch_bounds__(RO_THREADS, 1)
-readout_argmax_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ CUtensorMap mapBase,
                       const ReadoutParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + (size_t)p.kch * RO_A_CHUNK;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)p.stages * RO_B_STAGE);
-  uint64_t* a_full = bars;
-  uint64_t* b_full = bars + 1;
+  uint8_t* sB = smem;                                                  // stages x 16 KB
+  uint8_t* sBase = smem + (size_t)p.stages * RO_B_STAGE;               // RO_NBASE x 32 KB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sBase + (size_t)RO_NBASE * RO_BASE_TILE);
+  uint64_t* b_full = bars;
   uint64_t* b_empty = b_full + p.stages;
-  uint64_t* acc_full = b_empty + p.stages;
+  uint64_t* base_full = b_empty + p.stages;
+  uint64_t* base_empty = base_full + RO_NBASE;
+  uint64_t* acc_full = base_empty + RO_NBASE;
   uint64_t* acc_empty = acc_full + 2;
-  uint64_t* drain = acc_empty + 2;
+  uint64_t* a_ready = acc_empty + 2;
+  uint64_t* drain = a_ready + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   __shared__ int s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_tile = blockIdx.x % p.mt;
-  const int jslot = blockIdx.x / p.mt;
+  // blockIdx.x = ((jslot * mgroups) + mgroup) * cs + rank: the cs CTAs of a
+  // cluster hold consecutive M tiles and walk the same vocab tiles.
+  const int crank = (int)(blockIdx.x % p.cs);
+  const int mgroup = (int)((blockIdx.x / p.cs) % p.mgroups);
+  const int jslot = (int)(blockIdx.x / (p.cs * p.mgroups));
+  const int m_tile = mgroup * p.cs + crank;
+  const uint16_t cmask = (uint16_t)((1u << p.cs) - 1u);
   const int n_begin = (int)((int64_t)jslot * p.nt / p.per);
   const int n_end = (int)((int64_t)(jslot + 1) * p.nt / p.per);
   const int ntiles = n_end - n_begin;
 
   if (threadIdx.x == 0) {
-    mbar_init(a_full, 1);
     for (int s = 0; s < p.stages; ++s) {
-      mbar_init(&b_full[s], 1);
-      mbar_init(&b_empty[s], 1);
+      mbar_init(&b_full[s], 2);      // one arrive_expect_tx per W2 producer
+      mbar_init(&b_empty[s], p.cs);  // one release from every CTA of the cluster
+    }
+    for (int s = 0; s < RO_NBASE; ++s) {
+      mbar_init(&base_full[s], 1);
+      mbar_init(&base_empty[s], RO_EPI_WARPS);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], RO_EPI_WARPS);
     }
+    mbar_init(a_ready, RO_EPI_WARPS);
     mbar_init(drain, 1);
     fence_mbar_init();
   }
@@ -140,125 +148,199 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_con
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  // the peers' barriers must exist before any multicast lands in them
+  if (p.cs > 1)
+    cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ---------------- TMA producer ----------------
+  if (warp == 0 || warp == RO_WARP_W2B) {
+    // ---------------- TMA producers: W2 stages (one 64-column box each) ----
     if (lane == 0) {
-      prefetch_tensormap(&mapA);
-      prefetch_tensormap(&mapB);
-      mbar_arrive_expect_tx(a_full, (uint32_t)p.kch * RO_A_CHUNK);
-      for (int kc = 0; kc < p.kch; ++kc) tma_load_2d(sA + (size_t)kc * RO_A_CHUNK, &mapA, kc * RO_BK, m_tile * RO_BM, a_full);
+      const int half = warp == 0 ? 0 : 1;
+      if (half == 0) prefetch_tensormap(&mapW2);
       uint32_t it = 0;
       bool dead = false;
       for (int t = 0; t < ntiles && !dead; ++t) {
-        const int n0 = (n_begin + t) * RO_BN;
+        const int n0 = (n_begin + t) * RO_BN + half * 64;
         for (int kc = 0; kc < p.kch; ++kc, ++it) {
           const uint32_t s = it % p.stages, k = it / p.stages;
+          // stage s is free once every CTA of the cluster has consumed it
           if (k >= 1 && !mbar_wait(&b_empty[s], (k - 1) & 1)) {
             dead = true;
-            flag_error(p.hdr, XP_DEVERR_TIMEOUT);
             break;
           }
-          mbar_arrive_expect_tx(&b_full[s], RO_B_STAGE);
-          uint8_t* dst = sB + (size_t)s * RO_B_STAGE;
-#pragma unroll
-          for (int nb = 0; nb < RO_BN / 64; ++nb) tma_load_2d(dst + nb * RO_B_BOX, &mapB, n0 + nb * 64, kc * RO_BK, &b_full[s]);
+          mbar_arrive_expect_tx(&b_full[s], RO_BOX);
+          uint8_t* dst = sB + (size_t)s * RO_B_STAGE + half * RO_BOX;
+          if (p.cs == 1)
+            tma_load_2d(dst, &mapW2, n0, kc * RO_BK, &b_full[s]);
+          else if ((int)(it % p.cs) == crank)  // fetched once for the whole cluster
+            tma_load_2d_multicast(dst, &mapW2, n0, kc * RO_BK, &b_full[s], cmask);
         }
+      }
+      if (dead) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+    }
+  } else if (warp == RO_WARP_BASE) {
+    // ---------------- TMA producer: base tiles ----------------
+    if (lane == 0) {
+      prefetch_tensormap(&mapBase);
+      for (int t = 0; t < ntiles; ++t) {
+        const int n0 = (n_begin + t) * RO_BN;
+        const uint32_t bb = t % RO_NBASE, k = t / RO_NBASE;
+        if (k >= 1 && !mbar_wait(&base_empty[bb], (k - 1) & 1)) {
+          flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+          break;
+        }
+        mbar_arrive_expect_tx(&base_full[bb], RO_BASE_TILE);
+        uint8_t* dst = sBase + (size_t)bb * RO_BASE_TILE;
+        tma_load_2d(dst, &mapBase, n0, m_tile * RO_BM, &base_full[bb]);
+        tma_load_2d(dst + RO_BASE_BOX, &mapBase, n0 + 64, m_tile * RO_BM, &base_full[bb]);
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(RO_BM, RO_BN, 0, 1);
-      bool dead = !mbar_wait(a_full, 0);
-      if (dead) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+      bool dead = !mbar_wait(a_ready, 0);
       tc_fence_after();
       uint32_t it = 0;
       for (int t = 0; t < ntiles && !dead; ++t) {
         const uint32_t a = t & 1, u = t >> 1;
         if (u >= 1 && !mbar_wait(&acc_empty[a], (u - 1) & 1)) {
           dead = true;
-          flag_error(p.hdr, XP_DEVERR_TIMEOUT);
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem + a * RO_BN;
+        const uint32_t d = tmem + RO_TMEM_ACC + a * RO_BN;
         for (int kc = 0; kc < p.kch; ++kc, ++it) {
           const uint32_t s = it % p.stages, k = it / p.stages;
           if (!mbar_wait(&b_full[s], k & 1)) {
             dead = true;
-            flag_error(p.hdr, XP_DEVERR_TIMEOUT);
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + (size_t)kc * RO_A_CHUNK);
           const uint32_t b_base = smem_u32(sB + (size_t)s * RO_B_STAGE);
 #pragma unroll
           for (int kk = 0; kk < RO_BK / 16; ++kk) {
-            // A: K-major, 128-byte rows, 8-row groups 1024 B apart; a K step of
-            // 16 elements advances 32 bytes inside the swizzle atom.
-            const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
-            // B: N-major; 64-wide N blocks 8 KB apart (leading), 8-row K
-            // groups 1024 B apart (stride); a K step of 16 rows is 2 KB.
-            const uint64_t bdesc = smem_desc_sw128(b_base + kk * 2048, RO_B_BOX, 1024);
-            tc_mma_f16(d, adesc, bdesc, idesc, (kc | kk) != 0);
+            // A: TMEM columns hold K pairs; a K step of 16 is 8 columns.
+            const uint32_t a_tm = tmem + RO_TMEM_A + kc * 32 + kk * 8;
+            // B: N-major; 64-wide N blocks 8 KB apart (leading), 8-row K groups
+            // 1024 B apart (stride); a K step of 16 rows is 2 KB.
+            const uint64_t bdesc = smem_desc_sw128(b_base + kk * 2048, RO_BOX, 1024);
+            tc_mma_f16_ts(d, a_tm, bdesc, idesc, (kc | kk) != 0);
           }
-          tc_commit(&b_empty[s]);
+          if (p.cs == 1)
+            tc_commit(&b_empty[s]);
+          else
+            tc_commit_multicast(&b_empty[s], cmask);
         }
         if (dead) break;
         tc_commit(&acc_full[a]);
       }
-      // every MMA issued above has completed once this barrier fires
+      if (dead) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
       tc_commit(drain);
       (void)mbar_wait(drain, 0);
     }
-  } else {
-    // ---------------- epilogue ----------------
+  } else if (warp >= 2 && warp < 2 + RO_EPI_WARPS) {
+    // ---------------- epilogue warps ----------------
     const int q = warp & 3;          // TMEM lane quadrant this warp may access
-    const int h = (warp - 2) >> 2;   // 128-column half of the tile
-    const int row = m_tile * RO_BM + q * 32 + lane;
+    const int h = (warp - 2) >> 2;   // 64-column half of the tile
+    const int rr = q * 32 + lane;    // row within the M tile
+    const int row = m_tile * RO_BM + rr;
     const bool row_ok = row < p.rows;
-    const uint16_t* brow = p.base + (int64_t)(row_ok ? row : 0) * p.ld_base;
+    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+
+    // Stage the A operand (this row of the latent, zero-padded to 64*kch)
+    // into TMEM columns [0, 32*kch): the two warps of a lane quadrant split
+    // the K chunks, and each thread issues all of its loads before storing.
+    {
+      const uint16_t* arow = p.lat + (int64_t)(row_ok ? row : 0) * p.R;
+      const int kc0 = h * ((p.kch + 1) >> 1);
+      const int kc1 = h == 0 ? ((p.kch + 1) >> 1) : p.kch;
+      uint4 w[4][8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int k = (kc0 + i) * 64 + j * 8;  // first element of this 16-byte piece
+          w[i][j] = make_uint4(0, 0, 0, 0);
+          if (kc0 + i < kc1 && row_ok && k < p.R) w[i][j] = *reinterpret_cast<const uint4*>(arow + k);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (kc0 + i < kc1) {
+          uint32_t v[32];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            v[4 * j] = w[i][j].x;
+            v[4 * j + 1] = w[i][j].y;
+            v[4 * j + 2] = w[i][j].z;
+            v[4 * j + 3] = w[i][j].w;
+          }
+          tmem_st_32x32b_x32(tmem + lane_addr + RO_TMEM_A + (kc0 + i) * 32, v);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(a_ready);
+    }
+
     float best = -INFINITY;
     int bidx = -1;
     bool dead = false;
-    uint4 cur[16], nxt[16];
-    ro_load_base(cur, brow, n_begin * RO_BN + h * 128, p.V, row_ok);
     for (int t = 0; t < ntiles; ++t) {
       const uint32_t a = t & 1, u = t >> 1;
-      const int n0 = (n_begin + t) * RO_BN + h * 128;
-      if (t + 1 < ntiles) ro_load_base(nxt, brow, n0 + RO_BN, p.V, row_ok);
-      if (!dead && !mbar_wait(&acc_full[a], u & 1)) {
+      const uint32_t bb = t % RO_NBASE, kb = t / RO_NBASE;
+      const int n0 = (n_begin + t) * RO_BN + h * 64;
+      if (!dead && (!mbar_wait(&base_full[bb], kb & 1) || !mbar_wait(&acc_full[a], u & 1))) {
         dead = true;
         flag_error(p.hdr, XP_DEVERR_TIMEOUT);
       }
       tc_fence_after();
       if (!dead) {
-        const bool all_valid = n0 + 128 <= p.V;
+        const bool all_valid = n0 + 64 <= p.V;
+        // this row of the base box for columns [n0, n0+64): 128 bytes, its
+        // 16-byte chunks permuted by the 128-byte swizzle (chunk ^ row%8)
+        const uint8_t* brow = sBase + (size_t)bb * RO_BASE_TILE + (size_t)h * RO_BASE_BOX + (size_t)rr * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t r[32];
-          tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + a * RO_BN + h * 128 + c * 32, r);
+          tmem_ld_32x32b_x32(tmem + lane_addr + RO_TMEM_ACC + a * RO_BN + h * 64 + c * 32, r);
+          uint32_t bw[16];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint4 x = *reinterpret_cast<const uint4*>(brow + (((4 * c + v) ^ (rr & 7)) << 4));
+            bw[4 * v] = x.x;
+            bw[4 * v + 1] = x.y;
+            bw[4 * v + 2] = x.z;
+            bw[4 * v + 3] = x.w;
+          }
           tmem_ld_wait();
-          const uint4 bw[4] = {cur[4 * c], cur[4 * c + 1], cur[4 * c + 2], cur[4 * c + 3]};
           ro_chunk(r, bw, n0 + c * 32, p.V, all_valid, best, bidx);
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[a]);
-#pragma unroll
-      for (int v = 0; v < 16; ++v) cur[v] = nxt[v];
+      if (lane == 0) {
+        mbar_arrive(&acc_empty[a]);
+        mbar_arrive(&base_empty[bb]);
+      }
     }
     if (row_ok && bidx >= 0 && !dead) atomicMax(&p.keys[row], make_key(best, (uint32_t)bidx));
     __threadfence();
   }
 
   tc_fence_before();
-  __syncthreads();
+  // no CTA may leave while a peer can still multicast into it or arrive on
+  // its barriers
+  if (p.cs > 1)
+    cluster_sync();
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -287,40 +369,91 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_con
   }
 }
 
-size_t readout_smem_bytes(int kch, int stages) {
-  return 1024 + (size_t)kch * RO_A_CHUNK + (size_t)stages * RO_B_STAGE + 8 * (2 * stages + 6) + 16;
+size_t readout_smem_bytes(int stages) {
+  return 1024 + (size_t)stages * RO_B_STAGE + (size_t)RO_NBASE * RO_BASE_TILE +
+         8 * (2 * stages + 2 * RO_NBASE + 6) + 16;
 }
 
-xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2, const uint16_t* base, int64_t ld_base,
-                                int64_t rows, int64_t V, int64_t R, int64_t* blk, int64_t B, int32_t* changed,
-                                void* ws, cudaStream_t stream) {
+struct RoDevInfo {
+  bool init = false;
+  int sms = 0, max_smem = 0;
+  int active_clusters[9] = {0};  // by cluster size (1, 2, 4, 8)
+};
+static RoDevInfo g_ro_dev[64];
+
+// Cluster size for a given number of M tiles: the largest power of two <= 8
+// that divides into the tiles without leaving a whole idle CTA per cluster.
+int readout_cluster_size(int mt) {
+  if (mt >= 8) return 8;
+  if (mt >= 4) return 4;
+  if (mt >= 2) return 2;
+  return 1;
+}
+
+xp_status launch_readout_argmax_cs(const uint16_t* lat, const uint16_t* W2, const uint16_t* base, int64_t ld_base,
+                                   int64_t rows, int64_t V, int64_t R, int64_t* blk, int64_t B, int32_t* changed,
+                                   void* ws, cudaStream_t stream, int cs) {
   if (rows <= 0) return XP_OK;
   const int kch = (int)((R + RO_BK - 1) / RO_BK);
   if (kch > RO_MAX_KCH) return XP_ERR_SHAPE;
-  int dev = 0, sms = 0, max_smem = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-    return XP_ERR_LAUNCH;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return XP_ERR_LAUNCH;
+  RoDevInfo& info = g_ro_dev[dev];
+  if (!info.init) {
+    if (cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&info.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return XP_ERR_LAUNCH;
+    int stages = 8;
+    while (stages > 2 && readout_smem_bytes(stages) > (size_t)info.max_smem) --stages;
+    if (cudaFuncSetAttribute(readout_argmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)readout_smem_bytes(stages)) != cudaSuccess ||
+        cudaFuncSetAttribute(readout_argmax_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) !=
+            cudaSuccess)
+      return XP_ERR_LAUNCH;
+    for (int c = 1; c <= 8; c *= 2) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = c;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.gridDim = dim3(c * 64);
+      cfg.blockDim = dim3(RO_THREADS);
+      cfg.dynamicSmemBytes = readout_smem_bytes(stages);
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, readout_argmax_kernel, &cfg) != cudaSuccess) n = 0;
+      info.active_clusters[c] = n;
+    }
+    (void)cudaGetLastError();
+    info.init = true;
+  }
   int stages = 8;
-  while (stages > 2 && readout_smem_bytes(kch, stages) > (size_t)max_smem) --stages;
-  const size_t smem = readout_smem_bytes(kch, stages);
-  if (smem > (size_t)max_smem) return XP_ERR_SHAPE;
+  while (stages > 2 && readout_smem_bytes(stages) > (size_t)info.max_smem) --stages;
+  const size_t smem = readout_smem_bytes(stages);
+  if (smem > (size_t)info.max_smem) return XP_ERR_SHAPE;
 
-  CUtensorMap mapA, mapB;
-  if (!make_map_bf16_2d(&mapA, lat, (uint64_t)R, (uint64_t)rows, (uint64_t)R, RO_BK, RO_BM)) return XP_ERR_LAUNCH;
-  if (!make_map_bf16_2d(&mapB, W2, (uint64_t)V, (uint64_t)R, (uint64_t)V, 64, RO_BK)) return XP_ERR_LAUNCH;
+  CUtensorMap mapW2, mapBase;
+  if (!cached_map_bf16_2d(&mapW2, W2, (uint64_t)V, (uint64_t)R, (uint64_t)V, 64, RO_BK)) return XP_ERR_LAUNCH;
+  if (!cached_map_bf16_2d(&mapBase, base, (uint64_t)V, (uint64_t)rows, (uint64_t)ld_base, 64, RO_BM))
+    return XP_ERR_LAUNCH;
 
   ReadoutParams p;
   ArgmaxWs w = argmax_ws(ws, rows);
-  p.base = base;
-  p.ld_base = ld_base;
+  p.lat = lat;
   p.rows = (int32_t)rows;
   p.V = (int32_t)V;
+  p.R = (int32_t)R;
   p.kch = kch;
   p.mt = (int32_t)((rows + RO_BM - 1) / RO_BM);
   p.nt = (int32_t)((V + RO_BN - 1) / RO_BN);
-  int per = sms / p.mt;
+  if (cs < 1 || cs > 8 || (cs & (cs - 1))) cs = 1;
+  if (info.active_clusters[cs] <= 0) cs = 1;
+  p.cs = cs;
+  p.mgroups = (p.mt + cs - 1) / cs;
+  const int clusters = cs == 1 ? info.sms : info.active_clusters[cs];
+  int per = clusters / p.mgroups;
   if (per < 1) per = 1;
   if (per > p.nt) per = p.nt;
   p.per = per;
@@ -330,11 +463,29 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2, const u
   p.changed = changed;
   p.keys = w.keys;
   p.hdr = w.hdr;
-  if (cudaFuncSetAttribute(readout_argmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
-    return XP_ERR_LAUNCH;
-  readout_argmax_kernel<<<(unsigned int)(p.mt * per), RO_THREADS, smem, stream>>>(mapA, mapB, p);
-  return cudaGetLastError() == cudaSuccess ? XP_OK : XP_ERR_LAUNCH;
+
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = cs;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(per * p.mgroups * cs));
+  cfg.blockDim = dim3(RO_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, readout_argmax_kernel, mapW2, mapBase, p) != cudaSuccess) return XP_ERR_LAUNCH;
+  return XP_OK;
+}
+
+xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2, const uint16_t* base, int64_t ld_base,
+                                int64_t rows, int64_t V, int64_t R, int64_t* blk, int64_t B, int32_t* changed,
+                                void* ws, cudaStream_t stream) {
+  const int mt = (int)((rows + RO_BM - 1) / RO_BM);
+  return launch_readout_argmax_cs(lat, W2, base, ld_base, rows, V, R, blk, B, changed, ws, stream,
+                                  readout_cluster_size(mt));
 }
 
 }  // namespace xp

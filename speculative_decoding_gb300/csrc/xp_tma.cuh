@@ -40,4 +40,34 @@ inline bool make_map_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner, 
   return r == CUDA_SUCCESS;
 }
 
+// make_map_bf16_2d through a small per-thread cache keyed on every argument,
+// so repeated calls on the same buffers skip the encode.
+inline bool cached_map_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
+                               uint32_t box_inner, uint32_t box_outer) {
+  struct Entry {
+    const void* ptr;
+    uint64_t inner, outer, ld;
+    uint32_t bi, bo;
+    CUtensorMap map;
+  };
+  static thread_local Entry cache[16];
+  static thread_local unsigned next = 0;
+  for (auto& e : cache)
+    if (e.ptr == ptr && e.inner == inner && e.outer == outer && e.ld == ld && e.bi == box_inner &&
+        e.bo == box_outer) {
+      *map = e.map;
+      return true;
+    }
+  if (!make_map_bf16_2d(map, ptr, inner, outer, ld, box_inner, box_outer)) return false;
+  Entry& e = cache[next++ % 16];
+  e.ptr = ptr;
+  e.inner = inner;
+  e.outer = outer;
+  e.ld = ld;
+  e.bi = box_inner;
+  e.bo = box_outer;
+  e.map = *map;
+  return true;
+}
+
 }  // namespace xp
