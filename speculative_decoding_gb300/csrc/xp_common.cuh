@@ -80,7 +80,8 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
 struct WsHeader {
   unsigned int err;         // XP_DEVERR_* bits
   unsigned int done;        // CTAs of the current readout grid that finished
-  unsigned int pad[62];
+  unsigned int where;       // site code of the first wait that gave up (diagnostics)
+  unsigned int pad[61];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -129,5 +130,12 @@ __host__ inline LatentWsLayout latent_ws_layout(int64_t N, int64_t B, int64_t R,
 }
 
 __device__ __forceinline__ void flag_error(WsHeader* h, unsigned int bits) { atomicOr(&h->err, bits); }
+
+// a bounded wait gave up at `site`: set the timeout bit and remember the
+// first site
+__device__ __forceinline__ void flag_timeout(WsHeader* h, unsigned int site) {
+  atomicOr(&h->err, XP_DEVERR_TIMEOUT);
+  atomicCAS(&h->where, 0u, site);
+}
 
 }  // namespace xp

@@ -216,14 +216,22 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
       for (int bl = ks; bl < p.bpt; bl += p.S) {
         const int n = mt * p.bpt + bl;
         if (n >= p.N) break;
+        // all of the block's partial sums are requested before any is used,
+        // so the distributed-shared-memory latencies overlap
+        float v[LT_MAX_B][LT_MAX_S];
+#pragma unroll
+        for (int b = 0; b < LT_MAX_B; ++b)
+#pragma unroll
+          for (int q = 0; q < LT_MAX_S; ++q)
+            v[b][q] = (b < p.B && q < p.S) ? ld_dsmem_f32(&red[(bl * p.B + b) * red_ld + c], (uint32_t)q) : 0.f;
         float x[LT_MAX_B];
 #pragma unroll
         for (int b = 0; b < LT_MAX_B; ++b) {
           x[b] = 0.f;
           if (b < p.B) {
-            const int row = bl * p.B + b;
-            float acc = 0.f;
-            for (int q = 0; q < p.S; ++q) acc += ld_dsmem_f32(&red[row * red_ld + c], (uint32_t)q);
+            float acc = v[b][0];
+#pragma unroll
+            for (int q = 1; q < LT_MAX_S; ++q) acc += v[b][q];
             x[b] = bf2f(p.hcache[((int64_t)n * p.B + b) * p.R + col]) + acc;
           }
         }
@@ -483,15 +491,27 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
     const int col = nt * p.tn + c;
     if (c < p.tn && col < p.R) {
       const int r0 = ks * LT_BM / p.S, r1 = (ks + 1) * LT_BM / p.S;
-      for (int row = r0; row < r1; ++row) {
-        const int grow = mt * LT_BM + row;
-        if (grow >= rows) break;
-        const int n = grow / p.B, b = grow - n * p.B;
-        if (b == 0) continue;
-        float acc = 0.f;
-        for (int q = 0; q < p.S; ++q) acc += ld_dsmem_f32(&red[row * red_ld + c], (uint32_t)q);
-        const float y = p.u[(int64_t)grow * p.R + col] + acc;
-        p.lat[((int64_t)n * (p.B - 1) + b - 1) * p.R + col] = (uint16_t)(f32x2_to_bf16x2(y, 0.f) & 0xffffu);
+      // rows in groups of 8, every partial of a group requested before use
+      for (int g0 = r0; g0 < r1; g0 += 8) {
+        float v[8][LT_MAX_S];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int q = 0; q < LT_MAX_S; ++q)
+            v[i][q] = (g0 + i < r1 && q < p.S) ? ld_dsmem_f32(&red[(g0 + i) * red_ld + c], (uint32_t)q) : 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int row = g0 + i;
+          const int grow = mt * LT_BM + row;
+          if (row >= r1 || grow >= rows) break;
+          const int n = grow / p.B, b = grow - n * p.B;
+          if (b == 0) continue;
+          float acc = v[i][0];
+#pragma unroll
+          for (int q = 1; q < LT_MAX_S; ++q) acc += v[i][q];
+          const float y = p.u[(int64_t)grow * p.R + col] + acc;
+          p.lat[((int64_t)n * (p.B - 1) + b - 1) * p.R + col] = (uint16_t)(f32x2_to_bf16x2(y, 0.f) & 0xffffu);
+        }
       }
     }
   }

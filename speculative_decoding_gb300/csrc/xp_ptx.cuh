@@ -45,6 +45,18 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar_addr) : "memory");
 }
 
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
                    smem_u32(bar)),
@@ -144,9 +156,16 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
   asm volatile("mov.u32 %0, %cluster_nctarank;" : "=r"(r));
   return r;
 }
+// Cluster-wide barrier (every thread of every CTA of the cluster); the
+// .aligned forms need the warp converged, so reconverge first.
 __device__ __forceinline__ void cluster_sync() {
+  __syncwarp();
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// order this thread's earlier memory operations (including stores into peer
+// CTAs' shared memory) before its later ones, at cluster scope
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
 // shared::cta address -> the same offset in CTA `rank` of the cluster
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
@@ -161,6 +180,14 @@ __device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank)
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
   return v;
+}
+
+// store 16 bytes into the shared memory of CTA `rank` of the cluster, at the
+// offset of `local` in this CTA (made visible by the next cluster barrier)
+__device__ __forceinline__ void st_dsmem_v4(const void* local, uint32_t rank, float a, float b, float c, float d) {
+  const uint32_t addr = mapa_shared(smem_u32(local), rank);
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
 }
 
 // programmatic dependent launch: wait for the preceding kernel's results /

@@ -334,6 +334,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
     __threadfence();
   }
 
+  __syncwarp();  // lane-0 roles rejoin their warps before any .aligned op
   tc_fence_before();
   // no CTA may leave while a peer can still multicast into it or arrive on
   // its barriers
@@ -342,6 +343,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   else
     __syncthreads();
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
