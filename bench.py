@@ -243,7 +243,8 @@ def run_gb300(args, rank, world, local_rank):
     d = synth.pass_inputs(sh)
     # second set of per-pass inputs, alternated between steps
     d2 = synth.pass_inputs(synth.PassShape(sh.name, N, B, V, D, R, H, sh.seed + 100), with_embedding=False)
-    w = {k: dev_bf16(d[k], device) for k in ("E", "W_lat", "Wg", "Wu", "Wd", "W2")}
+    w = {k: dev_bf16(d[k], device) for k in ("E", "W_lat", "Wg", "Wu", "Wd")}
+    w["W2t"] = dev_bf16(np.ascontiguousarray(d["W2"].T), device)  # readout weight, vocabulary-major [V, R]
     L = torch.from_numpy(d["L"]).to(device)
     sets = []
     for src in (d, d2):
@@ -255,7 +256,7 @@ def run_gb300(args, rank, world, local_rank):
     def step(i):
         s = sets[i & 1]
         xpress.jacobi_pass(s["blk"], s["am1"], s["hcache"], w["E"], w["W_lat"], L, w["Wg"], w["Wu"], w["Wd"],
-                           w["W2"], s["base"], ws)
+                           w["W2t"], s["base"], ws)
 
     def reset():
         for s in sets:
@@ -291,7 +292,7 @@ def run_gb300(args, rank, world, local_rank):
         rblk = [s["blk"].clone() for s in sets]
 
         def ro(i):
-            xpress.readout_argmax(lat2, w["W2"], sets[i & 1]["base"], rblk[i & 1], rws)
+            xpress.readout_argmax(lat2, w["W2t"], sets[i & 1]["base"], rblk[i & 1], rws)
 
         for i in range(max(3, args.warmup)):
             ro(i)
@@ -324,7 +325,7 @@ def run_gb300(args, rank, world, local_rank):
             for k in ("hcache", "base", "am1", "blk"):
                 dev_in[k].copy_(h[k], non_blocking=True)
             xpress.jacobi_pass(dev_in["blk"], dev_in["am1"], dev_in["hcache"], w["E"], w["W_lat"], L, w["Wg"],
-                               w["Wu"], w["Wd"], w["W2"], dev_in["base"], ws)
+                               w["Wu"], w["Wd"], w["W2t"], dev_in["base"], ws)
             h["out"].copy_(dev_in["blk"], non_blocking=True)
 
         for i in range(max(3, args.warmup)):

@@ -122,17 +122,20 @@ XP_API xp_status xp_latent_pass(const int64_t* d_blk, const int64_t* d_am1, cons
  * its epilogue (the caller's `lat_out @ W2` followed by fused_add_argmax_to_blk,
  * without the bias or the logits ever reaching memory):
  *
- *   bias[r,v] = bf16(sum_k lat[r,k] * W2[k,v])              (fp32 accumulate)
+ *   bias[r,v] = bf16(sum_k lat[r,k] * W2t[v,k])             (fp32 accumulate)
  *   s[r,v]    = bf16(float(base[r*ld_base+v]) + float(bias[r,v]))
  *   blk[n*B + 1 + j] = lowest argmax_v s[r,v]               r = n*(B-1)+j
  *
- * d_lat [rows,R] bf16 dense, d_W2 [R,V] bf16 dense, d_base [rows,V] (ld_base).
- * R a multiple of 64, V a multiple of 8.  d_changed (nullable, device int32):
- * incremented by the number of slots whose token differs from the value blk
- * held before the call.  Workspace: xp_readout_workspace_size(rows, V).
+ * d_lat [rows,R] bf16 dense.  d_W2t [V,R] bf16 dense: the readout weight W2
+ * stored vocabulary-major (W2 transposed; the layout of a linear layer's
+ * weight), so one vocab tile's weights are contiguous.  d_base [rows,V] with
+ * row stride ld_base.  R a multiple of 8 in [8, 512].  d_changed (nullable,
+ * device int32): incremented by the number of slots whose token differs from
+ * the value blk held before the call.  Workspace:
+ * xp_readout_workspace_size(rows, V).
  * ---------------------------------------------------------------------- */
 XP_API size_t xp_readout_workspace_size(int64_t rows, int64_t V);
-XP_API xp_status xp_readout_argmax(const xp_bf16* d_lat, const xp_bf16* d_W2, const xp_bf16* d_base,
+XP_API xp_status xp_readout_argmax(const xp_bf16* d_lat, const xp_bf16* d_W2t, const xp_bf16* d_base,
                             int64_t ld_base, int64_t rows, int64_t V, int64_t R, int64_t* d_blk,
                             int64_t N, int64_t B, int32_t* d_changed, void* d_workspace,
                             size_t workspace_bytes, xp_stream_t stream);
@@ -142,7 +145,9 @@ XP_API xp_status xp_readout_argmax(const xp_bf16* d_lat, const xp_bf16* d_W2, co
  * its output (kept in the workspace), writing blk[:,1:] in place.  Repeated
  * calls iterate the Jacobi fixpoint: each pass reads the blk written by the
  * previous one (_xpress_add_argmax_reduce_to_blk_kernel docstring).
- * d_changed as in xp_readout_argmax.  Constraints: those of both stages.
+ * d_W2t [V,R] is the readout weight stored vocabulary-major, as in
+ * xp_readout_argmax.  d_changed as in xp_readout_argmax.  Constraints: those
+ * of both stages.
  * Workspace: xp_jacobi_workspace_size(N,B,V,D,R,H).
  * ---------------------------------------------------------------------- */
 XP_API size_t xp_jacobi_workspace_size(int64_t N, int64_t B, int64_t V, int64_t D, int64_t R, int64_t H);

@@ -75,20 +75,20 @@ size_t xp_readout_workspace_size(int64_t rows, int64_t V) {
   return xp::argmax_ws_bytes(rows);
 }
 
-xp_status xp_readout_argmax(const xp_bf16* d_lat, const xp_bf16* d_W2, const xp_bf16* d_base, int64_t ld_base,
+xp_status xp_readout_argmax(const xp_bf16* d_lat, const xp_bf16* d_W2t, const xp_bf16* d_base, int64_t ld_base,
                             int64_t rows, int64_t V, int64_t R, int64_t* d_blk, int64_t N, int64_t B,
                             int32_t* d_changed, void* d_workspace, size_t workspace_bytes, xp_stream_t stream) {
   if (N < 0 || B < 2 || V < 1 || V > (int64_t(1) << 30) || rows != N * (B - 1)) return XP_ERR_SHAPE;
   if (R < 8 || R > 512 || ld_base < V || rows > (int64_t(1) << 24)) return XP_ERR_SHAPE;
   if (rows == 0) return XP_OK;
-  if (!d_lat || !d_W2 || !d_base || !d_blk || !d_workspace) return XP_ERR_NULL;
-  if (!aligned16(d_lat) || !aligned16(d_W2) || !aligned16(d_base) || (ld_base & 7) || (V & 7) || (R & 7) ||
+  if (!d_lat || !d_W2t || !d_base || !d_blk || !d_workspace) return XP_ERR_NULL;
+  if (!aligned16(d_lat) || !aligned16(d_W2t) || !aligned16(d_base) || (ld_base & 7) || (R & 7) ||
       ((uintptr_t)d_blk & 7) || ((uintptr_t)d_changed & 3))
     return XP_ERR_ALIGN;
   if (!aligned256(d_workspace) || workspace_bytes < xp::argmax_ws_bytes(rows)) return XP_ERR_WORKSPACE;
   xp_status st = check_device();
   if (st != XP_OK) return st;
-  return xp::launch_readout_argmax(d_lat, d_W2, d_base, ld_base, rows, V, R, d_blk, B, d_changed, d_workspace,
+  return xp::launch_readout_argmax(d_lat, d_W2t, d_base, ld_base, rows, V, R, d_blk, B, d_changed, d_workspace,
                                    (cudaStream_t)stream);
 }
 
@@ -147,15 +147,14 @@ size_t xp_jacobi_workspace_size(int64_t N, int64_t B, int64_t V, int64_t D, int6
 
 xp_status xp_jacobi_pass(int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_hcache, const xp_bf16* d_E,
                          const xp_bf16* d_W_lat, const float* d_L, const xp_bf16* d_Wg, const xp_bf16* d_Wu,
-                         const xp_bf16* d_Wd, const xp_bf16* d_W2, const xp_bf16* d_base, int64_t ld_base, int64_t N,
+                         const xp_bf16* d_Wd, const xp_bf16* d_W2t, const xp_bf16* d_base, int64_t ld_base, int64_t N,
                          int64_t B, int64_t V, int64_t D, int64_t R, int64_t H, int32_t* d_changed,
                          void* d_workspace, size_t workspace_bytes, xp_stream_t stream) {
   xp_status st = check_latent_args(d_blk, d_am1, d_hcache, d_E, d_W_lat, d_L, d_Wg, d_Wu, d_Wd, N, B, V, D, R, H);
   if (st != XP_OK || N == 0) return st;
   if (ld_base < V) return XP_ERR_SHAPE;
-  if (!d_W2 || !d_base || !d_workspace) return XP_ERR_NULL;
-  if (!aligned16(d_W2) || !aligned16(d_base) || (ld_base & 7) || (V & 7) || ((uintptr_t)d_changed & 3))
-    return XP_ERR_ALIGN;
+  if (!d_W2t || !d_base || !d_workspace) return XP_ERR_NULL;
+  if (!aligned16(d_W2t) || !aligned16(d_base) || (ld_base & 7) || ((uintptr_t)d_changed & 3)) return XP_ERR_ALIGN;
   const xp::LatentWsLayout lay = xp::latent_ws_layout(N, B, R, H);
   if (!aligned256(d_workspace) || workspace_bytes < lay.total_pass) return XP_ERR_WORKSPACE;
   st = check_device();
@@ -164,7 +163,7 @@ xp_status xp_jacobi_pass(int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_
   st = xp::launch_latent(d_blk, d_am1, d_hcache, d_E, d_W_lat, d_L, d_Wg, d_Wu, d_Wd, lat, N, B, V, D, R, H,
                          d_workspace, (cudaStream_t)stream);
   if (st != XP_OK) return st;
-  return xp::launch_readout_argmax(lat, d_W2, d_base, ld_base, N * (B - 1), V, R, d_blk, B, d_changed, d_workspace,
+  return xp::launch_readout_argmax(lat, d_W2t, d_base, ld_base, N * (B - 1), V, R, d_blk, B, d_changed, d_workspace,
                                    (cudaStream_t)stream);
 }
 

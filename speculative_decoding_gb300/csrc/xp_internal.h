@@ -12,7 +12,7 @@ xp_status launch_add_argmax(const uint16_t* base, int64_t ld_base, const uint16_
                             int64_t rows, int64_t V, int64_t* blk, int64_t B, void* ws,
                             cudaStream_t stream);
 
-xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2, const uint16_t* base, int64_t ld_base,
+xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const uint16_t* base, int64_t ld_base,
                                 int64_t rows, int64_t V, int64_t R, int64_t* blk, int64_t B, int32_t* changed,
                                 void* ws, cudaStream_t stream);
 

@@ -10,14 +10,19 @@
 // reach memory.
 //
 // GB300 design (tcgen05 + TMEM + TMA):
+//   * W2 is read vocabulary-major (W2t = W2 transposed, [V, R]), so the
+//     weights of one 128-wide vocab tile are one contiguous 128 KB block of
+//     memory rather than 128-byte pieces of 512 distant rows;
 //   * one CTA per SM; CTA (m, j) owns M tile m (128 draft rows) and a
-//     contiguous range of 128-wide vocab tiles;
+//     contiguous range of vocab tiles;
 //   * the CTA's 128 x R slice of the latent (the MMA's A operand) is written
 //     ONCE into tensor memory (256 columns for R = 512) and every MMA reads
 //     it from there, which leaves shared memory to the streamed operands;
-//   * warp 0 (one thread) streams W2 in 64 x 128 K-chunks through a ring of
-//     stages and the matching 128 x 128 base tile into a second ring, all
-//     with TMA and 128-byte swizzle;
+//   * two producer threads (warps 0 and 10) stream W2t through a ring of
+//     4 stages of 128 vocab x 128 K (two 16 KB TMA boxes each), each owning
+//     alternate stages so their issue costs overlap; warp 11 streams the
+//     matching 128 x 128 base tile into a second ring (128-byte swizzle
+//     throughout);
 //   * warp 1 (one thread) issues tcgen05.mma M=128 N=128 K=16 (A in TMEM,
 //     B in shared memory, fp32 accumulate) into one of two 128-column TMEM
 //     accumulators, so the epilogue of tile t overlaps the MMAs of tile t+1;
@@ -38,29 +43,27 @@ namespace xp {
 
 constexpr int RO_BM = 128;
 constexpr int RO_BN = 128;
-constexpr int RO_BK = 64;
 constexpr int RO_EPI_WARPS = 8;
-// warp 0: W2 producer (left 64 columns of each stage); warp 1: MMA issuer;
-// warps 2..9: epilogue; warp 10: W2 producer (right 64 columns); warp 11:
-// base producer.  Several issuing threads keep more TMA transfers moving
-// than a single one can.
+// warp 0: W2 producer (even stages); warp 1: MMA issuer; warps 2..9:
+// epilogue; warp 10: W2 producer (odd stages); warp 11: base producer.
 constexpr int RO_WARP_W2B = 2 + RO_EPI_WARPS;
 constexpr int RO_WARP_BASE = RO_WARP_W2B + 1;
 constexpr int RO_THREADS = (RO_WARP_BASE + 1) * 32;
-constexpr uint32_t RO_BOX = 64 * 64 * 2;               // one 64 x 64 bf16 box (8 KB)
-constexpr uint32_t RO_B_STAGE = RO_BK * RO_BN * 2;     // W2 stage: 64 K x 128 N (16 KB)
+constexpr int RO_KS = 128;                             // K per W2 stage
+constexpr uint32_t RO_W2_BOX = 64 * RO_BN * 2;         // 64 K x 128 vocab (16 KB)
+constexpr uint32_t RO_B_STAGE = 2 * RO_W2_BOX;         // 32 KB
+constexpr int RO_STAGES = 4;                           // even: each producer owns fixed stages
 constexpr uint32_t RO_BASE_BOX = RO_BM * 64 * 2;       // base box: 128 rows x 64 cols (16 KB)
 constexpr uint32_t RO_BASE_TILE = RO_BM * RO_BN * 2;   // 32 KB
 constexpr int RO_NBASE = 2;
-constexpr int RO_MAX_KCH = 8;                          // R <= 512
+constexpr int RO_MAX_KCH = 8;                          // R <= 512 (K chunks of 64 in TMEM)
 constexpr uint32_t RO_TMEM_A = 0;                      // A: columns [0, 32*kch)
 constexpr uint32_t RO_TMEM_ACC = 256;                  // accumulators: [256, 384), [384, 512)
 
 struct ReadoutParams {
   const uint16_t* lat;
-  int32_t rows, V, R, kch, mt, nt, per, stages, B;
-  int32_t cs;       // CTAs per cluster: M tiles that share each W2 stage by multicast
-  int32_t mgroups;  // clusters along M (ceil(mt / cs))
+  int32_t rows, V, R, kch, mt, nt, per, B;
+  int32_t nks;      // W2 stages per tile: ceil(R / 128); kch = 2 * nks
   int64_t* blk;
   int32_t* changed;
   unsigned long long* keys;
@@ -101,11 +104,11 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sB = smem;                                                  // stages x 16 KB
-  uint8_t* sBase = smem + (size_t)p.stages * RO_B_STAGE;               // RO_NBASE x 32 KB
+  uint8_t* sBase = smem + (size_t)RO_STAGES * RO_B_STAGE;               // RO_NBASE x 32 KB
   uint64_t* bars = reinterpret_cast<uint64_t*>(sBase + (size_t)RO_NBASE * RO_BASE_TILE);
   uint64_t* b_full = bars;
-  uint64_t* b_empty = b_full + p.stages;
-  uint64_t* base_full = b_empty + p.stages;
+  uint64_t* b_empty = b_full + RO_STAGES;
+  uint64_t* base_full = b_empty + RO_STAGES;
   uint64_t* base_empty = base_full + RO_NBASE;
   uint64_t* acc_full = base_empty + RO_NBASE;
   uint64_t* acc_empty = acc_full + 2;
@@ -115,21 +118,16 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   __shared__ int s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // blockIdx.x = ((jslot * mgroups) + mgroup) * cs + rank: the cs CTAs of a
-  // cluster hold consecutive M tiles and walk the same vocab tiles.
-  const int crank = (int)(blockIdx.x % p.cs);
-  const int mgroup = (int)((blockIdx.x / p.cs) % p.mgroups);
-  const int jslot = (int)(blockIdx.x / (p.cs * p.mgroups));
-  const int m_tile = mgroup * p.cs + crank;
-  const uint16_t cmask = (uint16_t)((1u << p.cs) - 1u);
+  const int m_tile = (int)(blockIdx.x % p.mt);
+  const int jslot = (int)(blockIdx.x / p.mt);
   const int n_begin = (int)((int64_t)jslot * p.nt / p.per);
   const int n_end = (int)((int64_t)(jslot + 1) * p.nt / p.per);
   const int ntiles = n_end - n_begin;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < p.stages; ++s) {
-      mbar_init(&b_full[s], 2);      // one arrive_expect_tx per W2 producer
-      mbar_init(&b_empty[s], p.cs);  // one release from every CTA of the cluster
+    for (int s = 0; s < RO_STAGES; ++s) {
+      mbar_init(&b_full[s], 1);   // the owning W2 producer's arrive_expect_tx
+      mbar_init(&b_empty[s], 1);  // the MMA's release
     }
     for (int s = 0; s < RO_NBASE; ++s) {
       mbar_init(&base_full[s], 1);
@@ -148,36 +146,32 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
     tmem_relinquish();
   }
   tc_fence_before();
-  // the peers' barriers must exist before any multicast lands in them
-  if (p.cs > 1)
-    cluster_sync();
-  else
-    __syncthreads();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 || warp == RO_WARP_W2B) {
-    // ---------------- TMA producers: W2 stages (one 64-column box each) ----
+    // ---------------- TMA producers: W2t stages ----------------
+    // stage s (of RO_STAGES, even) is always refilled by producer s % 2, so
+    // each producer's waits on a stage follow that stage's uses in order
     if (lane == 0) {
-      const int half = warp == 0 ? 0 : 1;
-      if (half == 0) prefetch_tensormap(&mapW2);
+      const uint32_t pid = warp == 0 ? 0u : 1u;
+      if (pid == 0) prefetch_tensormap(&mapW2);
       uint32_t it = 0;
       bool dead = false;
       for (int t = 0; t < ntiles && !dead; ++t) {
-        const int n0 = (n_begin + t) * RO_BN + half * 64;
-        for (int kc = 0; kc < p.kch; ++kc, ++it) {
-          const uint32_t s = it % p.stages, k = it / p.stages;
-          // stage s is free once every CTA of the cluster has consumed it
+        const int n0 = (n_begin + t) * RO_BN;
+        for (int ks = 0; ks < p.nks; ++ks, ++it) {
+          const uint32_t s = it % RO_STAGES, k = it / RO_STAGES;
+          if ((s & 1u) != pid) continue;
           if (k >= 1 && !mbar_wait(&b_empty[s], (k - 1) & 1)) {
             dead = true;
             break;
           }
-          mbar_arrive_expect_tx(&b_full[s], RO_BOX);
-          uint8_t* dst = sB + (size_t)s * RO_B_STAGE + half * RO_BOX;
-          if (p.cs == 1)
-            tma_load_2d(dst, &mapW2, n0, kc * RO_BK, &b_full[s]);
-          else if ((int)(it % p.cs) == crank)  // fetched once for the whole cluster
-            tma_load_2d_multicast(dst, &mapW2, n0, kc * RO_BK, &b_full[s], cmask);
+          mbar_arrive_expect_tx(&b_full[s], RO_B_STAGE);
+          uint8_t* dst = sB + (size_t)s * RO_B_STAGE;
+          tma_load_2d(dst, &mapW2, ks * RO_KS, n0, &b_full[s]);
+          tma_load_2d(dst + RO_W2_BOX, &mapW2, ks * RO_KS + 64, n0, &b_full[s]);
         }
       }
       if (dead) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
@@ -202,7 +196,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(RO_BM, RO_BN, 0, 1);
+      constexpr uint32_t idesc = idesc_bf16_f32(RO_BM, RO_BN, 0, 0);
       bool dead = !mbar_wait(a_ready, 0);
       tc_fence_after();
       uint32_t it = 0;
@@ -214,27 +208,25 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
         }
         tc_fence_after();
         const uint32_t d = tmem + RO_TMEM_ACC + a * RO_BN;
-        for (int kc = 0; kc < p.kch; ++kc, ++it) {
-          const uint32_t s = it % p.stages, k = it / p.stages;
+        for (int ks = 0; ks < p.nks && !dead; ++ks, ++it) {
+          const uint32_t s = it % RO_STAGES, k = it / RO_STAGES;
           if (!mbar_wait(&b_full[s], k & 1)) {
             dead = true;
             break;
           }
           tc_fence_after();
           const uint32_t b_base = smem_u32(sB + (size_t)s * RO_B_STAGE);
-#pragma unroll
-          for (int kk = 0; kk < RO_BK / 16; ++kk) {
+          int ksteps = (p.R - ks * RO_KS + 15) / 16;
+          if (ksteps > RO_KS / 16) ksteps = RO_KS / 16;
+          for (int kk = 0; kk < ksteps; ++kk) {
             // A: TMEM columns hold K pairs; a K step of 16 is 8 columns.
-            const uint32_t a_tm = tmem + RO_TMEM_A + kc * 32 + kk * 8;
-            // B: N-major; 64-wide N blocks 8 KB apart (leading), 8-row K groups
-            // 1024 B apart (stride); a K step of 16 rows is 2 KB.
-            const uint64_t bdesc = smem_desc_sw128(b_base + kk * 2048, RO_BOX, 1024);
-            tc_mma_f16_ts(d, a_tm, bdesc, idesc, (kc | kk) != 0);
+            const uint32_t a_tm = tmem + RO_TMEM_A + ks * (RO_KS / 2) + kk * 8;
+            // B: K-major (W2t rows), 128-byte rows, 8-row groups 1024 B apart;
+            // a K step of 16 advances 32 bytes inside a 64-wide box.
+            const uint64_t bdesc = smem_desc_sw128(b_base + (kk >> 2) * RO_W2_BOX + (kk & 3) * 32, 16, 1024);
+            tc_mma_f16_ts(d, a_tm, bdesc, idesc, (ks | kk) != 0);
           }
-          if (p.cs == 1)
-            tc_commit(&b_empty[s]);
-          else
-            tc_commit_multicast(&b_empty[s], cmask);
+          tc_commit(&b_empty[s]);
         }
         if (dead) break;
         tc_commit(&acc_full[a]);
@@ -336,12 +328,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
 
   __syncwarp();  // lane-0 roles rejoin their warps before any .aligned op
   tc_fence_before();
-  // no CTA may leave while a peer can still multicast into it or arrive on
-  // its barriers
-  if (p.cs > 1)
-    cluster_sync();
-  else
-    __syncthreads();
+  __syncthreads();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -371,73 +358,43 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   }
 }
 
-size_t readout_smem_bytes(int stages) {
-  return 1024 + (size_t)stages * RO_B_STAGE + (size_t)RO_NBASE * RO_BASE_TILE +
-         8 * (2 * stages + 2 * RO_NBASE + 6) + 16;
+size_t readout_smem_bytes() {
+  return 1024 + (size_t)RO_STAGES * RO_B_STAGE + (size_t)RO_NBASE * RO_BASE_TILE +
+         8 * (2 * RO_STAGES + 2 * RO_NBASE + 6) + 16;
 }
 
+namespace {
 struct RoDevInfo {
   bool init = false;
-  int sms = 0, max_smem = 0;
-  int active_clusters[9] = {0};  // by cluster size (1, 2, 4, 8)
+  int sms = 0;
 };
-static RoDevInfo g_ro_dev[64];
+RoDevInfo g_ro_dev[64];
+}  // namespace
 
-// Cluster size for a given number of M tiles: the largest power of two <= 8
-// that divides into the tiles without leaving a whole idle CTA per cluster.
-int readout_cluster_size(int mt) {
-  if (mt >= 8) return 8;
-  if (mt >= 4) return 4;
-  if (mt >= 2) return 2;
-  return 1;
-}
-
-xp_status launch_readout_argmax_cs(const uint16_t* lat, const uint16_t* W2, const uint16_t* base, int64_t ld_base,
-                                   int64_t rows, int64_t V, int64_t R, int64_t* blk, int64_t B, int32_t* changed,
-                                   void* ws, cudaStream_t stream, int cs) {
+xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const uint16_t* base, int64_t ld_base,
+                                int64_t rows, int64_t V, int64_t R, int64_t* blk, int64_t B, int32_t* changed,
+                                void* ws, cudaStream_t stream) {
   if (rows <= 0) return XP_OK;
-  const int kch = (int)((R + RO_BK - 1) / RO_BK);
-  if (kch > RO_MAX_KCH) return XP_ERR_SHAPE;
+  const int nks = (int)((R + RO_KS - 1) / RO_KS);
+  if (2 * nks > RO_MAX_KCH) return XP_ERR_SHAPE;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return XP_ERR_LAUNCH;
   RoDevInfo& info = g_ro_dev[dev];
+  const size_t smem = readout_smem_bytes();
   if (!info.init) {
+    int max_smem = 0;
     if (cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&info.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
       return XP_ERR_LAUNCH;
-    int stages = 8;
-    while (stages > 2 && readout_smem_bytes(stages) > (size_t)info.max_smem) --stages;
-    if (cudaFuncSetAttribute(readout_argmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)readout_smem_bytes(stages)) != cudaSuccess ||
-        cudaFuncSetAttribute(readout_argmax_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) !=
-            cudaSuccess)
+    if (smem > (size_t)max_smem) return XP_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(readout_argmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
       return XP_ERR_LAUNCH;
-    for (int c = 1; c <= 8; c *= 2) {
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute attr;
-      attr.id = cudaLaunchAttributeClusterDimension;
-      attr.val.clusterDim.x = c;
-      attr.val.clusterDim.y = 1;
-      attr.val.clusterDim.z = 1;
-      cfg.gridDim = dim3(c * 64);
-      cfg.blockDim = dim3(RO_THREADS);
-      cfg.dynamicSmemBytes = readout_smem_bytes(stages);
-      cfg.attrs = &attr;
-      cfg.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, readout_argmax_kernel, &cfg) != cudaSuccess) n = 0;
-      info.active_clusters[c] = n;
-    }
-    (void)cudaGetLastError();
     info.init = true;
   }
-  int stages = 8;
-  while (stages > 2 && readout_smem_bytes(stages) > (size_t)info.max_smem) --stages;
-  const size_t smem = readout_smem_bytes(stages);
-  if (smem > (size_t)info.max_smem) return XP_ERR_SHAPE;
 
   CUtensorMap mapW2, mapBase;
-  if (!cached_map_bf16_2d(&mapW2, W2, (uint64_t)V, (uint64_t)R, (uint64_t)V, 64, RO_BK)) return XP_ERR_LAUNCH;
+  if (!cached_map_bf16_2d(&mapW2, W2t, (uint64_t)R, (uint64_t)V, (uint64_t)R, 64, RO_BN)) return XP_ERR_LAUNCH;
   if (!cached_map_bf16_2d(&mapBase, base, (uint64_t)V, (uint64_t)rows, (uint64_t)ld_base, 64, RO_BM))
     return XP_ERR_LAUNCH;
 
@@ -447,47 +404,21 @@ xp_status launch_readout_argmax_cs(const uint16_t* lat, const uint16_t* W2, cons
   p.rows = (int32_t)rows;
   p.V = (int32_t)V;
   p.R = (int32_t)R;
-  p.kch = kch;
+  p.nks = nks;
+  p.kch = 2 * nks;  // A staged in TMEM up to the last W2 stage, zero beyond R
   p.mt = (int32_t)((rows + RO_BM - 1) / RO_BM);
   p.nt = (int32_t)((V + RO_BN - 1) / RO_BN);
-  if (cs < 1 || cs > 8 || (cs & (cs - 1))) cs = 1;
-  if (info.active_clusters[cs] <= 0) cs = 1;
-  p.cs = cs;
-  p.mgroups = (p.mt + cs - 1) / cs;
-  const int clusters = cs == 1 ? info.sms : info.active_clusters[cs];
-  int per = clusters / p.mgroups;
+  int per = info.sms / p.mt;
   if (per < 1) per = 1;
   if (per > p.nt) per = p.nt;
   p.per = per;
-  p.stages = stages;
   p.B = (int32_t)B;
   p.blk = blk;
   p.changed = changed;
   p.keys = w.keys;
   p.hdr = w.hdr;
-
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = cs;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
-  cfg.gridDim = dim3((unsigned)(per * p.mgroups * cs));
-  cfg.blockDim = dim3(RO_THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, readout_argmax_kernel, mapW2, mapBase, p) != cudaSuccess) return XP_ERR_LAUNCH;
-  return XP_OK;
-}
-
-xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2, const uint16_t* base, int64_t ld_base,
-                                int64_t rows, int64_t V, int64_t R, int64_t* blk, int64_t B, int32_t* changed,
-                                void* ws, cudaStream_t stream) {
-  const int mt = (int)((rows + RO_BM - 1) / RO_BM);
-  return launch_readout_argmax_cs(lat, W2, base, ld_base, rows, V, R, blk, B, changed, ws, stream,
-                                  readout_cluster_size(mt));
+  readout_argmax_kernel<<<(unsigned int)(p.mt * per), RO_THREADS, smem, stream>>>(mapW2, mapBase, p);
+  return cudaGetLastError() == cudaSuccess ? XP_OK : XP_ERR_LAUNCH;
 }
 
 }  // namespace xp

@@ -146,12 +146,13 @@ def readout_workspace_size(rows: int, V: int) -> int:
     return int(lib().xp_readout_workspace_size(rows, V))
 
 
-def readout_argmax(lat, W2, base, blk, ws, changed=None, stream=None) -> None:
+def readout_argmax(lat, W2t, base, blk, ws, changed=None, stream=None) -> None:
+    """blk[n, 1+j] = lowest argmax_v bf16(base[r, v] + bf16(lat[r] . W2t[v])); W2t is [V, R]."""
     rows, R = lat.shape
-    V = W2.shape[1]
+    V = W2t.shape[0]
     N, B = blk.shape
     bf = torch.bfloat16
-    _check(lib().xp_readout_argmax(_ptr(lat, bf, "lat"), _ptr(W2, bf, "W2"),
+    _check(lib().xp_readout_argmax(_ptr(lat, bf, "lat"), _ptr(W2t, bf, "W2t"),
                                    _ptr(base, bf, "base", False), _rowmajor(base, "base"), rows, V, R,
                                    _ptr(blk, torch.int64, "blk"), N, B, _ptr(changed, torch.int32, "changed"),
                                    _ptr(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream)))
@@ -161,7 +162,8 @@ def jacobi_workspace_size(N: int, B: int, V: int, D: int, R: int, H: int) -> int
     return int(lib().xp_jacobi_workspace_size(N, B, V, D, R, H))
 
 
-def jacobi_pass(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, W2, base, ws, changed=None, stream=None) -> None:
+def jacobi_pass(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, W2t, base, ws, changed=None, stream=None) -> None:
+    """One pass in place on blk; W2t is the readout weight stored [V, R]."""
     N, B = blk.shape
     V, D = E.shape
     R = W_lat.shape[1]
@@ -170,7 +172,7 @@ def jacobi_pass(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, W2, base, ws, changed
     _check(lib().xp_jacobi_pass(_ptr(blk, torch.int64, "blk"), _ptr(am1, torch.int64, "am1"),
                                 _ptr(hcache, bf, "hcache"), _ptr(E, bf, "E"), _ptr(W_lat, bf, "W_lat"),
                                 _ptr(L, torch.float32, "L"), _ptr(Wg, bf, "Wg"), _ptr(Wu, bf, "Wu"),
-                                _ptr(Wd, bf, "Wd"), _ptr(W2, bf, "W2"), _ptr(base, bf, "base", False),
+                                _ptr(Wd, bf, "Wd"), _ptr(W2t, bf, "W2t"), _ptr(base, bf, "base", False),
                                 _rowmajor(base, "base"), N, B, V, D, R, H,
                                 _ptr(changed, torch.int32, "changed"),
                                 _ptr(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream)))

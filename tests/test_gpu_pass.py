@@ -24,7 +24,8 @@ class Pass:
     def __init__(self, d, shape):
         self.d, self.shape = d, shape
         N, B, V, D, R, H = shape.N, shape.B, shape.V, shape.D, shape.R, shape.H
-        self.t = {k: dev_bf16(d[k]) for k in ("hcache", "E", "W_lat", "Wg", "Wu", "Wd", "W2", "base")}
+        self.t = {k: dev_bf16(d[k]) for k in ("hcache", "E", "W_lat", "Wg", "Wu", "Wd", "base")}
+        self.t["W2t"] = dev_bf16(np.ascontiguousarray(d["W2"].T))  # the library's vocabulary-major layout
         self.am1 = dev(d["am1"])
         self.L = dev(d["L"])
         self.ws = xpress.workspace(xpress.jacobi_workspace_size(N, B, V, D, R, H))
@@ -35,7 +36,7 @@ class Pass:
         self.changed.zero_()
         t = self.t
         xpress.jacobi_pass(blk, self.am1, t["hcache"], t["E"], t["W_lat"], self.L, t["Wg"], t["Wu"], t["Wd"],
-                           t["W2"], t["base"], self.ws, changed=self.changed)
+                           t["W2t"], t["base"], self.ws, changed=self.changed)
         torch.cuda.synchronize()
         assert xpress.read_error(self.ws) == 0
         return blk.cpu().numpy(), int(self.changed.item())

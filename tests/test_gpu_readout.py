@@ -39,7 +39,8 @@ def _run(lat, W2, base, blk, ld=None):
     tblk = dev(blk.copy())
     changed = torch.zeros(1, dtype=torch.int32, device="cuda")
     ws = xpress.workspace(xpress.readout_workspace_size(rows, V))
-    xpress.readout_argmax(dev_bf16(lat), dev_bf16(W2), tb, tblk, ws, changed=changed)
+    # the library takes the readout weight vocabulary-major: W2t = W2.T, [V, R]
+    xpress.readout_argmax(dev_bf16(lat), dev_bf16(np.ascontiguousarray(W2.T)), tb, tblk, ws, changed=changed)
     torch.cuda.synchronize()
     assert xpress.read_error(ws) == 0
     assert int(ws[256:].count_nonzero().item()) == 0, "workspace not left clean"
