@@ -95,6 +95,37 @@ XP_API xp_status xp_add_argmax(const xp_bf16* d_base, int64_t ld_base, const xp_
                         int64_t B, void* d_workspace, size_t workspace_bytes, xp_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * xp_add_argmax_noalloc -- xp_add_argmax without a caller workspace.
+ * The XPress pages have no counterpart of this call: it only changes where
+ * the per-row scratch lives, not what is computed.  It is for callers that
+ * cannot hand out device memory per call: a serving engine that has given
+ * all free HBM to its KV-cache pool at start-up has nothing left to carve a
+ * workspace from, and code that must not call cudaMalloc/cudaFree (which
+ * synchronise the device and stall every other stream) cannot allocate one.
+ *
+ * Same arguments, result and errors as xp_add_argmax, minus the workspace.
+ * The scratch (one 64-bit key and one counter per row) is a fixed array in
+ * the library's device memory, sized for XP_ADD_ARGMAX_NOALLOC_MAX_ROWS rows;
+ * rows above that return XP_ERR_SHAPE before anything is launched.  Each call
+ * zeroes the part of the scratch it uses (cudaMemsetAsync on `stream`) and
+ * then launches the add-argmax kernel; it calls no allocator.
+ *
+ * The first call on each device (with that device current) looks up the
+ * scratch's device address, which may load the library's device code; make
+ * that first call before any stream capture.  Later calls only read the
+ * cached address.
+ *
+ * There is one scratch per device: calls that can overlap in time (on
+ * different streams without ordering between them, or from several host
+ * threads) race on it and corrupt each other's results.  Serialise them,
+ * e.g. issue them all on one stream.
+ * ---------------------------------------------------------------------- */
+#define XP_ADD_ARGMAX_NOALLOC_MAX_ROWS 8192
+XP_API xp_status xp_add_argmax_noalloc(const xp_bf16* d_base, int64_t ld_base, const xp_bf16* d_bias,
+                                int64_t ld_bias, int64_t rows, int64_t V, int64_t* d_blk, int64_t N,
+                                int64_t B, xp_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * xp_latent_pass -- the fused latent stage.
  * Pages: xpress_latent_pass / _xpress_latent_kernel (in-kernel MLP form).
  *

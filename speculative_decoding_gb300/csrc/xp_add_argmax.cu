@@ -15,6 +15,9 @@
 // last CTA of a row (arrival counter) writes blk and re-zeroes the key and
 // counter, so the workspace is clean for the next call and no second launch
 // or partial buffer is needed.
+#include <atomic>
+#include <mutex>
+
 #include "xp_common.cuh"
 #include "xp_internal.h"
 
@@ -134,6 +137,57 @@ xp_status launch_add_argmax(const uint16_t* base, int64_t ld_base, const uint16_
   add_argmax_kernel<AA_THREADS, AA_VEC><<<(unsigned int)grid, AA_THREADS, 0, stream>>>(
       base, ld_base, bias, ld_bias, (int32_t)V, (int32_t)nchunks, blk, (int32_t)B, w.keys, w.cnt);
   return cudaGetLastError() == cudaSuccess ? XP_OK : XP_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the keys and counters live in one fixed array of
+// device memory per device instead of a caller workspace.  Its layout is the
+// workspace layout of argmax_ws() for up to XP_ADD_ARGMAX_NOALLOC_MAX_ROWS rows.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoallocBytes = 256 + ((8 * (size_t)XP_ADD_ARGMAX_NOALLOC_MAX_ROWS + 255) & ~size_t(255)) +
+                                 ((4 * (size_t)XP_ADD_ARGMAX_NOALLOC_MAX_ROWS + 255) & ~size_t(255));
+static __device__ __align__(256) unsigned char g_add_argmax_scratch[kNoallocBytes];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<void*> g_scratch_ptr[kMaxDevices];
+std::mutex g_scratch_mu;
+
+// Device address of this device's scratch; looked up once per device with
+// that device current (the lookup may load this module's device code).
+xp_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return XP_ERR_LAUNCH;
+  if (dev < 0 || dev >= kMaxDevices) return XP_ERR_UNSUPPORTED;
+  void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+    if (p == nullptr) {
+      if (cudaGetSymbolAddress(&p, g_add_argmax_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();  // do not leave the lookup's error for the next call to find
+        return XP_ERR_LAUNCH;
+      }
+      g_scratch_ptr[dev].store(p, std::memory_order_release);
+    }
+  }
+  *out = p;
+  return XP_OK;
+}
+}  // namespace
+
+xp_status launch_add_argmax_noalloc(const uint16_t* base, int64_t ld_base, const uint16_t* bias, int64_t ld_bias,
+                                    int64_t rows, int64_t V, int64_t* blk, int64_t B, cudaStream_t stream) {
+  if (rows < 0 || rows > XP_ADD_ARGMAX_NOALLOC_MAX_ROWS) return XP_ERR_SHAPE;
+  if (rows == 0) return XP_OK;
+  void* ws = nullptr;
+  xp_status st = noalloc_scratch(&ws);
+  if (st != XP_OK) return st;
+  // keys and counters must start at zero; the kernel leaves them zero, but a
+  // call that never completed (an error, a killed stream) could have left
+  // them dirty, so clear the rows this call uses
+  if (cudaMemsetAsync(ws, 0, argmax_ws_bytes(rows), stream) != cudaSuccess) return XP_ERR_LAUNCH;
+  return launch_add_argmax(base, ld_base, bias, ld_bias, rows, V, blk, B, ws, stream);
 }
 
 }  // namespace xp

@@ -69,6 +69,19 @@ xp_status xp_add_argmax(const xp_bf16* d_base, int64_t ld_base, const xp_bf16* d
                                (cudaStream_t)stream);
 }
 
+xp_status xp_add_argmax_noalloc(const xp_bf16* d_base, int64_t ld_base, const xp_bf16* d_bias, int64_t ld_bias,
+                                int64_t rows, int64_t V, int64_t* d_blk, int64_t N, int64_t B, xp_stream_t stream) {
+  if (N < 0 || B < 2 || V < 1 || V > (int64_t(1) << 30) || rows != N * (B - 1)) return XP_ERR_SHAPE;
+  if (ld_base < V || ld_bias < V || rows > XP_ADD_ARGMAX_NOALLOC_MAX_ROWS) return XP_ERR_SHAPE;
+  if (rows == 0) return XP_OK;
+  if (!d_base || !d_bias || !d_blk) return XP_ERR_NULL;
+  if (!aligned16(d_base) || !aligned16(d_bias) || (ld_base & 7) || (ld_bias & 7) || ((uintptr_t)d_blk & 7))
+    return XP_ERR_ALIGN;
+  xp_status st = check_device();
+  if (st != XP_OK) return st;
+  return xp::launch_add_argmax_noalloc(d_base, ld_base, d_bias, ld_bias, rows, V, d_blk, B, (cudaStream_t)stream);
+}
+
 size_t xp_readout_workspace_size(int64_t rows, int64_t V) {
   (void)V;
   if (rows < 0) return 0;

@@ -12,6 +12,10 @@ xp_status launch_add_argmax(const uint16_t* base, int64_t ld_base, const uint16_
                             int64_t rows, int64_t V, int64_t* blk, int64_t B, void* ws,
                             cudaStream_t stream);
 
+// xp_add_argmax on the library's fixed per-device scratch (no workspace).
+xp_status launch_add_argmax_noalloc(const uint16_t* base, int64_t ld_base, const uint16_t* bias, int64_t ld_bias,
+                                    int64_t rows, int64_t V, int64_t* blk, int64_t B, cudaStream_t stream);
+
 xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const uint16_t* base, int64_t ld_base,
                                 int64_t rows, int64_t V, int64_t R, int64_t* blk, int64_t B, int32_t* changed,
                                 void* ws, cudaStream_t stream);

@@ -20,6 +20,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "xpress.h")
 
 XP_OK, XP_ERR_NULL, XP_ERR_SHAPE, XP_ERR_ALIGN, XP_ERR_WORKSPACE, XP_ERR_LAUNCH, XP_ERR_UNSUPPORTED = range(7)
 XP_DEVERR_TOKEN, XP_DEVERR_TIMEOUT = 1, 2
+NOALLOC_MAX_ROWS = 8192  # XP_ADD_ARGMAX_NOALLOC_MAX_ROWS
 
 
 class XpressError(RuntimeError):
@@ -38,6 +39,7 @@ _SIGS = {
     "xp_version": (ctypes.c_int32, []),
     "xp_add_argmax_workspace_size": (_sz, [_i64, _i64]),
     "xp_add_argmax": (ctypes.c_int32, [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _sz, _vp]),
+    "xp_add_argmax_noalloc": (ctypes.c_int32, [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp]),
     "xp_latent_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _i64]),
     "xp_latent_pass": (ctypes.c_int32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                         _i64, _i64, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
@@ -123,6 +125,16 @@ def add_argmax(base, bias, blk, ws, stream=None) -> None:
                                _ptr(bias, torch.bfloat16, "bias", False), _rowmajor(bias, "bias"),
                                rows, V, _ptr(blk, torch.int64, "blk"), N, B,
                                _ptr(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream)))
+
+
+def add_argmax_noalloc(base, bias, blk, stream=None) -> None:
+    """add_argmax on the library's fixed scratch: no workspace, at most
+    NOALLOC_MAX_ROWS rows, and calls that overlap in time race."""
+    rows, V = base.shape
+    N, B = blk.shape
+    _check(lib().xp_add_argmax_noalloc(_ptr(base, torch.bfloat16, "base", False), _rowmajor(base, "base"),
+                                       _ptr(bias, torch.bfloat16, "bias", False), _rowmajor(bias, "bias"),
+                                       rows, V, _ptr(blk, torch.int64, "blk"), N, B, _stream(stream)))
 
 
 def latent_workspace_size(N: int, B: int, D: int, R: int, H: int) -> int:
