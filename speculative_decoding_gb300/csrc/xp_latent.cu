@@ -50,6 +50,11 @@ __device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float((uint
 // ============================================================================
 // proj_mix: x = hcache + E[prev] @ W_lat, then the causal mixer
 // ============================================================================
+// Shared memory: [0, region) is the stage ring; once the MMAs are done it holds
+// red[128][tn + 4] (this CTA's fp32 partial sums, read by the whole cluster)
+// and xs[128][w] (the reduced x of this CTA's w columns).  After it: Ls (the
+// mixer weights of those columns, lower triangle packed by rows), the token
+// table and the barriers.
 struct ProjParams {
   const int64_t* blk;
   const int64_t* am1;
@@ -59,23 +64,29 @@ struct ProjParams {
   float* u;
   uint16_t* ub;
   WsHeader* hdr;
-  int32_t N, B, V, D, R, bpt, tn, S, chunks, ntiles, stages;
+  int32_t N, B, V, D, R, bpt, tn, S, w, chunks, ntiles, stages;
+  uint32_t region;
 };
 
-__global__ void __launch_bounds__(LT_THREADS, 1)
+__host__ __device__ inline uint32_t proj_ls_bytes(int B, int w) {
+  return (uint32_t)(((B * (B + 1) / 2) * w * 4 + 15) & ~15);
+}
+
+__global__ void __launch_bounds__(LT_THREADS, 2)
 proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const uint32_t b_bytes = (uint32_t)p.tn * LT_BK * 2;
   const uint32_t stage_bytes = LT_A_CHUNK + b_bytes;
-  const int red_ld = p.tn + 1;  // padded row of the partial-sum buffer
-  const size_t ring = (size_t)p.stages * stage_bytes;
-  const size_t red_bytes = (size_t)LT_BM * red_ld * 4;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (ring > red_bytes ? ring : red_bytes));
+  const int ld = p.tn + 4;  // floats per row of red (a 16-byte multiple)
+  float* red = reinterpret_cast<float*>(smem);
+  float* xs = red + LT_BM * ld;
+  float* Ls = reinterpret_cast<float*>(smem + p.region);
+  int64_t* tok = reinterpret_cast<int64_t*>(smem + p.region + proj_ls_bytes(p.B, p.w));
+  uint64_t* full = reinterpret_cast<uint64_t*>(tok + LT_BM);
   uint64_t* empty = full + p.stages;
   uint64_t* acc_full = empty + p.stages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
-  float* red = reinterpret_cast<float*>(smem);  // reuses the ring once the MMAs are done
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ks = (int)(blockIdx.x % p.S);
@@ -83,6 +94,9 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
   const int mt = (int)(blockIdx.x / (p.S * p.ntiles));
   const int c0 = (int)((int64_t)ks * p.chunks / p.S);
   const int nck = (int)((int64_t)(ks + 1) * p.chunks / p.S) - c0;
+  const int c_lo = ks * p.w;                   // this CTA's columns of the tile: [c_lo, c_lo + w)
+  const int col0 = nt * p.tn + c_lo;           // ... as latent channels
+  const int nbl = min(p.bpt, p.N - mt * p.bpt);  // blocks of this M tile
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -104,19 +118,24 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
   pdl_wait();  // blk may have been written by the preceding pass
 
   if (warp == 0) {
-    if (lane == 0) {
-      prefetch_tensormap(&mapWlat);
-      for (int i = 0; i < nck; ++i) {
-        const uint32_t s = i % p.stages, k = i / p.stages;
-        if (k >= 1 && !mbar_wait(&empty[s], (k - 1) & 1)) {
-          flag_error(p.hdr, XP_DEVERR_TIMEOUT);
-          break;
-        }
-        mbar_arrive_expect_tx(&full[s], b_bytes);
-        uint8_t* dst = smem + (size_t)s * stage_bytes + LT_A_CHUNK;
-        for (int bx = 0; bx < p.tn / 64; ++bx)
-          tma_load_2d(dst + bx * LT_BOX, &mapWlat, nt * p.tn + bx * 64, (c0 + i) * LT_BK, &full[s]);
+    // lane 0 waits for the stage and arms its barrier; lanes 0..tn/64-1 then
+    // issue one W_lat box each (a single thread issues tiled copies slowly)
+    if (lane == 0) prefetch_tensormap(&mapWlat);
+    for (int i = 0; i < nck; ++i) {
+      const uint32_t s = i % p.stages, k = i / p.stages;
+      int ok = 1;
+      if (lane == 0) {
+        if (k >= 1 && !mbar_wait(&empty[s], (k - 1) & 1)) ok = 0;
+        else mbar_arrive_expect_tx(&full[s], b_bytes);
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+        break;
+      }
+      if (lane < p.tn / 64)
+        tma_load_2d(smem + (size_t)s * stage_bytes + LT_A_CHUNK + lane * LT_BOX, &mapWlat, nt * p.tn + lane * 64,
+                    (c0 + i) * LT_BK, &full[s]);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -143,56 +162,63 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
       tc_commit(acc_full);
     }
   } else {
-    // gather: warp gw fills chunks i = gw, gw+4, ...; lane owns rows lane+32j
-    const int gw = warp - 2;
-    int64_t prev[4];
-    bool valid[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int r = lane + 32 * j;
-      const int bl = r / p.B, b = r - bl * p.B;
-      const int n = mt * p.bpt + bl;
-      valid[j] = bl < p.bpt && n < p.N;
-      prev[j] = 0;
-      if (valid[j]) {
-        int64_t t = (b == 0) ? p.am1[n] : p.blk[(int64_t)n * p.B + b - 1];
+    const int et = threadIdx.x - 64;  // 0..127
+    // token of every row of the tile (-1: no block there)
+    {
+      const int bl = et / p.B, b = et - bl * p.B, n = mt * p.bpt + bl;
+      int64_t t = -1;
+      if (bl < nbl) {
+        t = (b == 0) ? p.am1[n] : p.blk[(int64_t)n * p.B + b - 1];
         if (t < 0 || t >= p.V) {
           flag_error(p.hdr, XP_DEVERR_TOKEN);
           t = t < 0 ? 0 : p.V - 1;
         }
-        prev[j] = t;
       }
+      tok[et] = t;
     }
-    for (int i = gw; i < nck; i += 4) {
-      const uint32_t s = i % p.stages, k = i / p.stages;
+    named_barrier_sync(1, 128);
+    // gather: warp gw owns the stages s with s % 4 == gw and refills them in
+    // order.  Eight lanes cover one 128-byte row piece, so each copy
+    // instruction reads four whole rows; cp.async keeps all 32 copies of a
+    // lane in flight without registers.
+    const int gw = warp - 2, rsub = lane >> 3, piece = lane & 7;
+    for (int i = 0; i < nck; ++i) {
+      const int s = i % p.stages;
+      if (s % 4 != gw) continue;
+      const int k = i / p.stages;
       if (k >= 1 && !mbar_wait(&empty[s], (k - 1) & 1)) {
         flag_error(p.hdr, XP_DEVERR_TIMEOUT);
         break;
       }
       uint8_t* dst = smem + (size_t)s * stage_bytes;
-      const int kel0 = (c0 + i) * LT_BK;
-      uint4 v[4][8];
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          v[j][c] = make_uint4(0, 0, 0, 0);
-          if (valid[j] && kel0 + 8 * c < p.D)
-            v[j][c] = *reinterpret_cast<const uint4*>(p.E + prev[j] * p.D + kel0 + 8 * c);
-        }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int r = lane + 32 * j;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = v[j][c];
+      const int kel = (c0 + i) * LT_BK + piece * 8;
+      const bool kin = kel < p.D;  // D is a multiple of 8: a piece is wholly in or out
+#pragma unroll 8
+      for (int it = 0; it < LT_BM / 4; ++it) {
+        const int r = it * 4 + rsub;
+        const int64_t t = tok[r];
+        const bool ok = kin && t >= 0;
+        cp_async_16(dst + r * 128 + ((piece ^ (r & 7)) << 4), ok ? p.E + t * p.D + kel : p.E, ok ? 16u : 0u);
       }
+      cp_async_wait_all();
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[s]);
     }
+    // the mixer weights of this CTA's columns, copied in the background while
+    // the MMAs finish (waited for before the mixer)
+    const int tri = p.B * (p.B + 1) / 2;
+    for (int e = et; e < tri * p.w; e += 128) {
+      const int pr = e / p.w, c = e - pr * p.w;
+      int b = 0;
+      while ((b + 1) * (b + 2) / 2 <= pr) ++b;
+      const int j = pr - b * (b + 1) / 2;
+      const bool in = col0 + c < p.R;
+      cp_async_4(Ls + e, in ? p.L + ((int64_t)b * p.B + j) * p.R + col0 + c : p.L, in ? 4u : 0u);
+    }
   }
 
-  // ---- epilogue 1: the partial sums TMEM -> shared memory (warps 2..5)
+  // ---- epilogue 1: the partial sums TMEM -> red (warps 2..5, one row each)
   if (warp >= 2) {
     if (!mbar_wait(acc_full, 0)) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
     tc_fence_after();
@@ -201,55 +227,90 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
       uint32_t r[32];
       tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + c * 32, r);
       tmem_ld_wait();
+      float4* dst = reinterpret_cast<float4*>(red + row * ld + c * 32);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) red[row * red_ld + c * 32 + e] = __uint_as_float(r[e]);
+      for (int e = 0; e < 8; ++e)
+        dst[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]), __uint_as_float(r[4 * e + 2]),
+                             __uint_as_float(r[4 * e + 3]));
     }
   }
   tc_fence_before();
   cluster_sync();
 
-  // ---- epilogue 2: sum the cluster's partials, add hcache, causal mixer
-  if (threadIdx.x >= 64) {
-    const int c = threadIdx.x - 64;
-    const int col = nt * p.tn + c;
-    if (c < p.tn && col < p.R) {
-      for (int bl = ks; bl < p.bpt; bl += p.S) {
-        const int n = mt * p.bpt + bl;
-        if (n >= p.N) break;
-        // all of the block's partial sums are requested before any is used,
-        // so the distributed-shared-memory latencies overlap
-        float v[LT_MAX_B][LT_MAX_S];
+  if (warp >= 2) {
+    const int et = threadIdx.x - 64;
+    // ---- epilogue 2: x = hcache + sum of the cluster's partials (fixed
+    // order) for this CTA's columns of all rows; two (row, 4 columns) items
+    // per thread per round, every partial requested before any is used
+    const int wq = p.w / 4, items = LT_BM * wq;
+    for (int i0 = et; i0 < items; i0 += 256) {
+      float4 v[2][LT_MAX_S];
+      uint2 hc[2];
+      int rr[2], gg[2];
+      bool on[2];
 #pragma unroll
-        for (int b = 0; b < LT_MAX_B; ++b)
+      for (int h = 0; h < 2; ++h) {
+        const int it = i0 + h * 128;
+        rr[h] = it / wq;
+        gg[h] = it - rr[h] * wq;
+        const int bl = rr[h] / p.B, b = rr[h] - bl * p.B;
+        on[h] = it < items && bl < nbl;
+        const int col = col0 + 4 * gg[h];
+        hc[h] = make_uint2(0u, 0u);
+        if (on[h] && col < p.R)
+          hc[h] = *reinterpret_cast<const uint2*>(p.hcache + ((int64_t)(mt * p.bpt + bl) * p.B + b) * p.R + col);
 #pragma unroll
-          for (int q = 0; q < LT_MAX_S; ++q)
-            v[b][q] = (b < p.B && q < p.S) ? ld_dsmem_f32(&red[(bl * p.B + b) * red_ld + c], (uint32_t)q) : 0.f;
-        float x[LT_MAX_B];
+        for (int q = 0; q < LT_MAX_S; ++q)
+          v[h][q] = (on[h] && q < p.S) ? ld_dsmem_v4(red + rr[h] * ld + c_lo + 4 * gg[h], (uint32_t)q)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
 #pragma unroll
-        for (int b = 0; b < LT_MAX_B; ++b) {
-          x[b] = 0.f;
-          if (b < p.B) {
-            float acc = v[b][0];
+      for (int h = 0; h < 2; ++h) {
+        if (!on[h]) continue;
+        float4 a = v[h][0];
 #pragma unroll
-            for (int q = 1; q < LT_MAX_S; ++q) acc += v[b][q];
-            x[b] = bf2f(p.hcache[((int64_t)n * p.B + b) * p.R + col]) + acc;
+        for (int q = 1; q < LT_MAX_S; ++q) {
+          if (q < p.S) {
+            a.x += v[h][q].x;
+            a.y += v[h][q].y;
+            a.z += v[h][q].z;
+            a.w += v[h][q].w;
           }
         }
+        float4 x;
+        x.x = bf16lo_to_f32(hc[h].x) + a.x;
+        x.y = bf16hi_to_f32(hc[h].x) + a.y;
+        x.z = bf16lo_to_f32(hc[h].y) + a.z;
+        x.w = bf16hi_to_f32(hc[h].y) + a.w;
+        *reinterpret_cast<float4*>(xs + rr[h] * p.w + 4 * gg[h]) = x;
+      }
+    }
+    cp_async_wait_all();  // this thread's share of Ls
+    named_barrier_sync(1, 128);
+    // ---- the causal mixer on this CTA's columns: u[b] = sum_{j<=b} L[b,j] x[j]
+    for (int it = et; it < nbl * p.w; it += 128) {
+      const int bl = it / p.w, c = it - bl * p.w;
+      const int col = col0 + c;
+      if (col >= p.R) continue;
+      const int n = mt * p.bpt + bl;
+      float x[LT_MAX_B];
 #pragma unroll
-        for (int b = 0; b < LT_MAX_B; ++b) {
-          if (b < p.B) {
-            float uu = 0.f;
+      for (int j = 0; j < LT_MAX_B; ++j) x[j] = j < p.B ? xs[(bl * p.B + j) * p.w + c] : 0.f;
 #pragma unroll
-            for (int j = 0; j <= b; ++j) uu = fmaf(p.L[((int64_t)b * p.B + j) * p.R + col], x[j], uu);
-            const int64_t o = ((int64_t)n * p.B + b) * p.R + col;
-            p.u[o] = uu;
-            p.ub[o] = (uint16_t)(f32x2_to_bf16x2(uu, 0.f) & 0xffffu);
-          }
+      for (int b = 0; b < LT_MAX_B; ++b) {
+        if (b < p.B) {
+          float uu = 0.f;
+          const float* Lb = Ls + (b * (b + 1) / 2) * p.w + c;
+#pragma unroll
+          for (int j = 0; j <= b; ++j) uu = fmaf(Lb[j * p.w], x[j], uu);
+          const int64_t o = ((int64_t)n * p.B + b) * p.R + col;
+          p.u[o] = uu;
+          p.ub[o] = (uint16_t)(f32x2_to_bf16x2(uu, 0.f) & 0xffffu);
         }
       }
     }
   }
-  cluster_sync();  // the peers have finished reading this CTA's partials
+  cluster_sync();  // the peers have finished reading this CTA's partial sums
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 128);
@@ -300,22 +361,28 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
   pdl_wait();  // ub comes from proj_mix
 
   if (warp == 0) {
+    // lane 0 arms the stage; lanes 0, 1, 2 issue the ub, Wg and Wu boxes
     if (lane == 0) {
       prefetch_tensormap(&mapUb);
       prefetch_tensormap(&mapWg);
       prefetch_tensormap(&mapWu);
-      for (int i = 0; i < p.chunks; ++i) {
-        const uint32_t s = i % p.stages, k = i / p.stages;
-        if (k >= 1 && !mbar_wait(&empty[s], (k - 1) & 1)) {
-          flag_error(p.hdr, XP_DEVERR_TIMEOUT);
-          break;
-        }
-        mbar_arrive_expect_tx(&full[s], stage_bytes);
-        uint8_t* dst = smem + (size_t)s * stage_bytes;
-        tma_load_2d(dst, &mapUb, i * LT_BK, mt * LT_BM, &full[s]);
-        tma_load_2d(dst + LT_A_CHUNK, &mapWg, ht * 64, i * LT_BK, &full[s]);
-        tma_load_2d(dst + LT_A_CHUNK + LT_BOX, &mapWu, ht * 64, i * LT_BK, &full[s]);
+    }
+    for (int i = 0; i < p.chunks; ++i) {
+      const uint32_t s = i % p.stages, k = i / p.stages;
+      int ok = 1;
+      if (lane == 0) {
+        if (k >= 1 && !mbar_wait(&empty[s], (k - 1) & 1)) ok = 0;
+        else mbar_arrive_expect_tx(&full[s], stage_bytes);
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+        break;
+      }
+      uint8_t* dst = smem + (size_t)s * stage_bytes;
+      if (lane == 0) tma_load_2d(dst, &mapUb, i * LT_BK, mt * LT_BM, &full[s]);
+      if (lane == 1) tma_load_2d(dst + LT_A_CHUNK, &mapWg, ht * 64, i * LT_BK, &full[s]);
+      if (lane == 2) tma_load_2d(dst + LT_A_CHUNK + LT_BOX, &mapWu, ht * 64, i * LT_BK, &full[s]);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -358,8 +425,8 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const float g0 = __uint_as_float(g[2 * e]), g1 = __uint_as_float(g[2 * e + 1]);
-          const float m0 = g0 / (1.f + expf(-g0)) * __uint_as_float(v[2 * e]);
-          const float m1 = g1 / (1.f + expf(-g1)) * __uint_as_float(v[2 * e + 1]);
+          const float m0 = __fdividef(g0, 1.f + __expf(-g0)) * __uint_as_float(v[2 * e]);
+          const float m1 = __fdividef(g1, 1.f + __expf(-g1)) * __uint_as_float(v[2 * e + 1]);
           w[e] = f32x2_to_bf16x2(m0, m1);
         }
         uint4* dst = reinterpret_cast<uint4*>(p.m + (int64_t)row * p.H + ht * 64 + c * 32);
@@ -379,24 +446,25 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
 // ============================================================================
 // mlp_down: lat = bf16(u + m @ Wd) for slots 1..B-1
 // ============================================================================
+// Shared memory: [0, region) is the stage ring, then red[128][tn + 4] (this
+// CTA's fp32 partial sums, read by the whole cluster); barriers after it.
 struct DownParams {
   const float* u;
   uint16_t* lat;
   WsHeader* hdr;
-  int32_t N, B, R, tn, S, chunks, ntiles, stages;
+  int32_t N, B, R, tn, S, w, chunks, ntiles, stages;
+  uint32_t region;
 };
 
-__global__ void __launch_bounds__(LT_THREADS, 1)
+__global__ void __launch_bounds__(LT_THREADS, 2)
 mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant__ CUtensorMap mapWd,
                 const DownParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const uint32_t b_bytes = (uint32_t)p.tn * LT_BK * 2;
   const uint32_t stage_bytes = LT_A_CHUNK + b_bytes;
-  const int red_ld = p.tn + 1;
-  const size_t ring = (size_t)p.stages * stage_bytes;
-  const size_t red_bytes = (size_t)LT_BM * red_ld * 4;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (ring > red_bytes ? ring : red_bytes));
+  const int ld = p.tn + 4;  // floats per row of red (a 16-byte multiple)
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.region);
   uint64_t* empty = full + p.stages;
   uint64_t* acc_full = empty + p.stages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
@@ -409,6 +477,8 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
   const int c0 = (int)((int64_t)ks * p.chunks / p.S);
   const int nck = (int)((int64_t)(ks + 1) * p.chunks / p.S) - c0;
   const int rows = p.N * p.B;
+  const int c_lo = ks * p.w;          // this CTA's columns of the tile: [c_lo, c_lo + w)
+  const int col0 = nt * p.tn + c_lo;  // ... as latent channels
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -430,21 +500,28 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
   pdl_wait();  // m comes from mlp_up
 
   if (warp == 0) {
+    // lane 0 arms the stage; lane 0 issues the m box, lanes 1.. the Wd boxes
     if (lane == 0) {
       prefetch_tensormap(&mapM);
       prefetch_tensormap(&mapWd);
-      for (int i = 0; i < nck; ++i) {
-        const uint32_t s = i % p.stages, k = i / p.stages;
-        if (k >= 1 && !mbar_wait(&empty[s], (k - 1) & 1)) {
-          flag_error(p.hdr, XP_DEVERR_TIMEOUT);
-          break;
-        }
-        mbar_arrive_expect_tx(&full[s], stage_bytes);
-        uint8_t* dst = smem + (size_t)s * stage_bytes;
-        tma_load_2d(dst, &mapM, (c0 + i) * LT_BK, mt * LT_BM, &full[s]);
-        for (int bx = 0; bx < p.tn / 64; ++bx)
-          tma_load_2d(dst + LT_A_CHUNK + bx * LT_BOX, &mapWd, nt * p.tn + bx * 64, (c0 + i) * LT_BK, &full[s]);
+    }
+    for (int i = 0; i < nck; ++i) {
+      const uint32_t s = i % p.stages, k = i / p.stages;
+      int ok = 1;
+      if (lane == 0) {
+        if (k >= 1 && !mbar_wait(&empty[s], (k - 1) & 1)) ok = 0;
+        else mbar_arrive_expect_tx(&full[s], stage_bytes);
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+        break;
+      }
+      uint8_t* dst = smem + (size_t)s * stage_bytes;
+      if (lane == 0) tma_load_2d(dst, &mapM, (c0 + i) * LT_BK, mt * LT_BM, &full[s]);
+      if (lane >= 1 && lane <= p.tn / 64)
+        tma_load_2d(dst + LT_A_CHUNK + (lane - 1) * LT_BOX, &mapWd, nt * p.tn + (lane - 1) * 64, (c0 + i) * LT_BK,
+                    &full[s]);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -478,40 +555,57 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
       uint32_t r[32];
       tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + c * 32, r);
       tmem_ld_wait();
+      float4* dst = reinterpret_cast<float4*>(red + row * ld + c * 32);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) red[row * red_ld + c * 32 + e] = __uint_as_float(r[e]);
+      for (int e = 0; e < 8; ++e)
+        dst[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]), __uint_as_float(r[4 * e + 2]),
+                             __uint_as_float(r[4 * e + 3]));
     }
   }
   tc_fence_before();
   cluster_sync();
 
-  // ---- sum the cluster's partials, add the residual, write slots 1..B-1
-  if (threadIdx.x >= 64) {
-    const int c = threadIdx.x - 64;
-    const int col = nt * p.tn + c;
-    if (c < p.tn && col < p.R) {
-      const int r0 = ks * LT_BM / p.S, r1 = (ks + 1) * LT_BM / p.S;
-      // rows in groups of 8, every partial of a group requested before use
-      for (int g0 = r0; g0 < r1; g0 += 8) {
-        float v[8][LT_MAX_S];
+  // ---- sum the cluster's partials for this CTA's columns (fixed order), add
+  // the residual u, write slots 1..B-1.  Two (row, 4 columns) items per
+  // thread per round; the residual and every partial are requested first.
+  if (warp >= 2) {
+    const int et = threadIdx.x - 64;
+    const int wq = p.w / 4, items = LT_BM * wq;
+    for (int i0 = et; i0 < items; i0 += 256) {
+      float4 v[2][LT_MAX_S], uu[2];
+      int64_t dst[2];
+      bool on[2];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+      for (int h = 0; h < 2; ++h) {
+        const int it = i0 + h * 128;
+        const int rr = it / wq, gg = it - rr * wq;
+        const int grow = mt * LT_BM + rr;
+        const int n = grow / p.B, b = grow - n * p.B;
+        const int col = col0 + 4 * gg;
+        on[h] = it < items && grow < rows && b >= 1 && col < p.R;
+        dst[h] = ((int64_t)n * (p.B - 1) + b - 1) * p.R + col;
+        uu[h] = on[h] ? *reinterpret_cast<const float4*>(p.u + (int64_t)grow * p.R + col)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int q = 0; q < LT_MAX_S; ++q)
-            v[i][q] = (g0 + i < r1 && q < p.S) ? ld_dsmem_f32(&red[(g0 + i) * red_ld + c], (uint32_t)q) : 0.f;
+        for (int q = 0; q < LT_MAX_S; ++q)
+          v[h][q] = (on[h] && q < p.S) ? ld_dsmem_v4(red + rr * ld + c_lo + 4 * gg, (uint32_t)q)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int row = g0 + i;
-          const int grow = mt * LT_BM + row;
-          if (row >= r1 || grow >= rows) break;
-          const int n = grow / p.B, b = grow - n * p.B;
-          if (b == 0) continue;
-          float acc = v[i][0];
+      for (int h = 0; h < 2; ++h) {
+        if (!on[h]) continue;
+        float4 a = v[h][0];
 #pragma unroll
-          for (int q = 1; q < LT_MAX_S; ++q) acc += v[i][q];
-          const float y = p.u[(int64_t)grow * p.R + col] + acc;
-          p.lat[((int64_t)n * (p.B - 1) + b - 1) * p.R + col] = (uint16_t)(f32x2_to_bf16x2(y, 0.f) & 0xffffu);
+        for (int q = 1; q < LT_MAX_S; ++q) {
+          if (q < p.S) {
+            a.x += v[h][q].x;
+            a.y += v[h][q].y;
+            a.z += v[h][q].z;
+            a.w += v[h][q].w;
+          }
         }
+        *reinterpret_cast<uint2*>(p.lat + dst[h]) =
+            make_uint2(f32x2_to_bf16x2(uu[h].x + a.x, uu[h].y + a.y), f32x2_to_bf16x2(uu[h].z + a.z, uu[h].w + a.w));
       }
     }
   }
@@ -550,10 +644,27 @@ cudaError_t launch_ex(const void* kernel_fn, dim3 grid, size_t smem, cudaStream_
   return cudaLaunchKernelExC(&cfg, kernel_fn, args);
 }
 
-int pick_stages(uint32_t stage_bytes, int chunks_per_cta, size_t min_ring) {
+// Largest power of two <= min(cap, x) (x >= 1): the cluster size of a split
+// reduction, so every CTA's column slice of a tile is a multiple of 4 wide.
+int pow2_floor(int x, int cap) {
+  int s = 1;
+  while (s * 2 <= x && s * 2 <= cap) s *= 2;
+  return s;
+}
+
+// Dynamic shared memory that still lets two CTAs share an SM: 228 KB per SM,
+// 1 KB of it reserved per CTA, with some margin.
+constexpr size_t kTwoPerSm = 112 * 1024;
+
+// Stage count for a ring of `stage_bytes` stages: deep enough for the CTA's
+// chunks (at most 6), then cut back (not below 2) until `total(stages)` fits
+// two CTAs per SM.
+template <class F>
+int pick_stages(uint32_t stage_bytes, int chunks_per_cta, F total) {
   int st = chunks_per_cta < 6 ? chunks_per_cta : 6;
   if (st < 2) st = 2;
-  while ((size_t)st * stage_bytes < min_ring) ++st;
+  while (st > 2 && total(st) > kTwoPerSm) --st;
+  (void)stage_bytes;
   return st;
 }
 
@@ -574,11 +685,14 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     int max_smem = 0;
     if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
       return XP_ERR_LAUNCH;
+    // the largest shared-memory carve-out, so two ~110 KB CTAs fit an SM
     if (cudaFuncSetAttribute(proj_mix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
             cudaSuccess ||
         cudaFuncSetAttribute(mlp_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) != cudaSuccess ||
         cudaFuncSetAttribute(mlp_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
-            cudaSuccess)
+            cudaSuccess ||
+        cudaFuncSetAttribute(proj_mix_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess ||
+        cudaFuncSetAttribute(mlp_down_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
       return XP_ERR_LAUNCH;
     g_lt_attr[dev] = true;
   }
@@ -611,12 +725,21 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     p.bpt = (int32_t)(LT_BM / B);
     p.tn = tn;
     p.chunks = (int32_t)((D + LT_BK - 1) / LT_BK);
-    p.S = p.chunks < LT_MAX_S ? p.chunks : LT_MAX_S;
+    p.S = pow2_floor(p.chunks, LT_MAX_S);
+    p.w = tn / p.S;
     p.ntiles = ntiles;
     const uint32_t stage_bytes = LT_A_CHUNK + (uint32_t)tn * LT_BK * 2;
+    const size_t red_xs = (size_t)LT_BM * (tn + 4) * 4 + (size_t)LT_BM * p.w * 4;
+    const size_t tail = proj_ls_bytes((int)B, p.w) + 8 * LT_BM;  // Ls + token table
+    auto region_of = [&](int st) {
+      const size_t ring = (size_t)st * stage_bytes;
+      return (ring > red_xs ? ring : red_xs + 1023) & ~size_t(1023);
+    };
+    auto total = [&](int st) { return 1024 + region_of(st) + tail + 8 * (2 * st + 1) + 16; };
     const int per_cta = (p.chunks + p.S - 1) / p.S;
-    p.stages = pick_stages(stage_bytes, per_cta, (size_t)LT_BM * (tn + 1) * 4);
-    const size_t smem = 1024 + (size_t)p.stages * stage_bytes + 8 * (2 * p.stages + 1) + 16;
+    p.stages = pick_stages(stage_bytes, per_cta, total);
+    p.region = (uint32_t)region_of(p.stages);
+    const size_t smem = total(p.stages);
     const int mtiles = (int)((N + p.bpt - 1) / p.bpt);
     CUtensorMap mapWlat;
     if (!cached_map_bf16_2d(&mapWlat, W_lat, (uint64_t)R, (uint64_t)D, (uint64_t)R, 64, LT_BK)) return XP_ERR_LAUNCH;
@@ -634,7 +757,7 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     p.H = (int32_t)H;
     p.chunks = (int32_t)((R + LT_BK - 1) / LT_BK);
     p.htiles = (int32_t)(H / 64);
-    p.stages = pick_stages(LT_A_CHUNK + 2 * LT_BOX, p.chunks, 0);
+    p.stages = p.chunks < 6 ? (p.chunks < 2 ? 2 : p.chunks) : 6;
     const size_t smem = 1024 + (size_t)p.stages * (LT_A_CHUNK + 2 * LT_BOX) + 8 * (2 * p.stages + 1) + 16;
     const int mtiles = (rows + LT_BM - 1) / LT_BM;
     CUtensorMap mapUb, mapWg, mapWu;
@@ -658,12 +781,20 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     p.R = (int32_t)R;
     p.tn = tn;
     p.chunks = (int32_t)(H / LT_BK);
-    p.S = p.chunks < LT_MAX_S ? p.chunks : LT_MAX_S;
+    p.S = pow2_floor(p.chunks, LT_MAX_S);
+    p.w = tn / p.S;
     p.ntiles = ntiles;
     const uint32_t stage_bytes = LT_A_CHUNK + (uint32_t)tn * LT_BK * 2;
+    const size_t red_bytes = (size_t)LT_BM * (tn + 4) * 4;
+    auto region_of = [&](int st) {
+      const size_t ring = (size_t)st * stage_bytes;
+      return (ring > red_bytes ? ring : red_bytes + 1023) & ~size_t(1023);
+    };
+    auto total = [&](int st) { return 1024 + region_of(st) + 8 * (2 * st + 1) + 16; };
     const int per_cta = (p.chunks + p.S - 1) / p.S;
-    p.stages = pick_stages(stage_bytes, per_cta, (size_t)LT_BM * (tn + 1) * 4);
-    const size_t smem = 1024 + (size_t)p.stages * stage_bytes + 8 * (2 * p.stages + 1) + 16;
+    p.stages = pick_stages(stage_bytes, per_cta, total);
+    p.region = (uint32_t)region_of(p.stages);
+    const size_t smem = total(p.stages);
     const int mtiles = (rows + LT_BM - 1) / LT_BM;
     CUtensorMap mapM, mapWd;
     if (!cached_map_bf16_2d(&mapM, m, (uint64_t)H, (uint64_t)rows, (uint64_t)H, LT_BK, LT_BM) ||

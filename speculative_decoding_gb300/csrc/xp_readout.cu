@@ -52,7 +52,7 @@ constexpr int RO_THREADS = (RO_WARP_BASE + 1) * 32;
 constexpr int RO_KS = 128;                             // K per W2 stage
 constexpr uint32_t RO_W2_BOX = 64 * RO_BN * 2;         // 64 K x 128 vocab (16 KB)
 constexpr uint32_t RO_B_STAGE = 2 * RO_W2_BOX;         // 32 KB
-constexpr int RO_STAGES = 4;                           // even: each producer owns fixed stages
+constexpr int RO_STAGES = 5;                           // stage s is always refilled by producer s % 2
 constexpr uint32_t RO_BASE_BOX = RO_BM * 64 * 2;       // base box: 128 rows x 64 cols (16 KB)
 constexpr uint32_t RO_BASE_TILE = RO_BM * RO_BN * 2;   // 32 KB
 constexpr int RO_NBASE = 2;
@@ -152,46 +152,51 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
 
   if (warp == 0 || warp == RO_WARP_W2B) {
     // ---------------- TMA producers: W2t stages ----------------
-    // stage s (of RO_STAGES, even) is always refilled by producer s % 2, so
-    // each producer's waits on a stage follow that stage's uses in order
-    if (lane == 0) {
-      const uint32_t pid = warp == 0 ? 0u : 1u;
-      if (pid == 0) prefetch_tensormap(&mapW2);
-      uint32_t it = 0;
-      bool dead = false;
-      for (int t = 0; t < ntiles && !dead; ++t) {
-        const int n0 = (n_begin + t) * RO_BN;
-        for (int ks = 0; ks < p.nks; ++ks, ++it) {
-          const uint32_t s = it % RO_STAGES, k = it / RO_STAGES;
-          if ((s & 1u) != pid) continue;
-          if (k >= 1 && !mbar_wait(&b_empty[s], (k - 1) & 1)) {
-            dead = true;
-            break;
-          }
-          mbar_arrive_expect_tx(&b_full[s], RO_B_STAGE);
-          uint8_t* dst = sB + (size_t)s * RO_B_STAGE;
-          tma_load_2d(dst, &mapW2, ks * RO_KS, n0, &b_full[s]);
-          tma_load_2d(dst + RO_W2_BOX, &mapW2, ks * RO_KS + 64, n0, &b_full[s]);
+    // stage s is always refilled by producer s % 2, so each producer's waits
+    // on a stage follow that stage's uses in order.  Lane 0 waits for the
+    // stage and arms its barrier; lanes 0 and 1 issue one box each (a single
+    // thread issues tiled copies slowly)
+    const uint32_t pid = warp == 0 ? 0u : 1u;
+    if (pid == 0 && lane == 0) prefetch_tensormap(&mapW2);
+    uint32_t it = 0;
+    bool dead = false;
+    for (int t = 0; t < ntiles && !dead; ++t) {
+      const int n0 = (n_begin + t) * RO_BN;
+      for (int ks = 0; ks < p.nks; ++ks, ++it) {
+        const uint32_t s = it % RO_STAGES, k = it / RO_STAGES;
+        if ((s & 1u) != pid) continue;
+        int ok = 1;
+        if (lane == 0) {
+          if (k >= 1 && !mbar_wait(&b_empty[s], (k - 1) & 1)) ok = 0;
+          else mbar_arrive_expect_tx(&b_full[s], RO_B_STAGE);
         }
-      }
-      if (dead) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
-    }
-  } else if (warp == RO_WARP_BASE) {
-    // ---------------- TMA producer: base tiles ----------------
-    if (lane == 0) {
-      prefetch_tensormap(&mapBase);
-      for (int t = 0; t < ntiles; ++t) {
-        const int n0 = (n_begin + t) * RO_BN;
-        const uint32_t bb = t % RO_NBASE, k = t / RO_NBASE;
-        if (k >= 1 && !mbar_wait(&base_empty[bb], (k - 1) & 1)) {
-          flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          dead = true;
           break;
         }
-        mbar_arrive_expect_tx(&base_full[bb], RO_BASE_TILE);
-        uint8_t* dst = sBase + (size_t)bb * RO_BASE_TILE;
-        tma_load_2d(dst, &mapBase, n0, m_tile * RO_BM, &base_full[bb]);
-        tma_load_2d(dst + RO_BASE_BOX, &mapBase, n0 + 64, m_tile * RO_BM, &base_full[bb]);
+        if (lane < 2) tma_load_2d(sB + (size_t)s * RO_B_STAGE + lane * RO_W2_BOX, &mapW2, ks * RO_KS + lane * 64, n0,
+                                  &b_full[s]);
       }
+    }
+    if (dead && lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+  } else if (warp == RO_WARP_BASE) {
+    // ---------------- TMA producer: base tiles (two lanes, one box each) ----------------
+    if (lane == 0) prefetch_tensormap(&mapBase);
+    for (int t = 0; t < ntiles; ++t) {
+      const int n0 = (n_begin + t) * RO_BN;
+      const uint32_t bb = t % RO_NBASE, k = t / RO_NBASE;
+      int ok = 1;
+      if (lane == 0) {
+        if (k >= 1 && !mbar_wait(&base_empty[bb], (k - 1) & 1)) ok = 0;
+        else mbar_arrive_expect_tx(&base_full[bb], RO_BASE_TILE);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        if (lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+        break;
+      }
+      if (lane < 2)
+        tma_load_2d(sBase + (size_t)bb * RO_BASE_TILE + lane * RO_BASE_BOX, &mapBase, n0 + lane * 64,
+                    m_tile * RO_BM, &base_full[bb]);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
@@ -364,6 +369,21 @@ size_t readout_smem_bytes() {
 }
 
 namespace {
+// Work split: mt M tiles of 128 rows x per contiguous vocabulary ranges of
+// 128-wide tiles, one CTA each (mt * per <= SMs).
+struct RoSplit {
+  int32_t mt, nt, per;
+};
+RoSplit readout_split(int sms, int64_t rows, int64_t V) {
+  RoSplit s;
+  s.mt = (int32_t)((rows + RO_BM - 1) / RO_BM);
+  s.nt = (int32_t)((V + RO_BN - 1) / RO_BN);
+  s.per = sms / s.mt;
+  if (s.per < 1) s.per = 1;
+  if (s.per > s.nt) s.per = s.nt;
+  return s;
+}
+
 struct RoDevInfo {
   bool init = false;
   int sms = 0;
@@ -400,18 +420,17 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
 
   ReadoutParams p;
   ArgmaxWs w = argmax_ws(ws, rows);
+  const RoSplit sp = readout_split(info.sms, rows, V);
   p.lat = lat;
   p.rows = (int32_t)rows;
   p.V = (int32_t)V;
   p.R = (int32_t)R;
   p.nks = nks;
   p.kch = 2 * nks;  // A staged in TMEM up to the last W2 stage, zero beyond R
-  p.mt = (int32_t)((rows + RO_BM - 1) / RO_BM);
-  p.nt = (int32_t)((V + RO_BN - 1) / RO_BN);
-  int per = info.sms / p.mt;
-  if (per < 1) per = 1;
-  if (per > p.nt) per = p.nt;
-  p.per = per;
+  p.mt = sp.mt;
+  p.nt = sp.nt;
+  p.per = sp.per;
+  const int per = sp.per;
   p.B = (int32_t)B;
   p.blk = blk;
   p.changed = changed;
