@@ -87,7 +87,7 @@ XP_API int32_t xp_version(void);
  * -0 and +0 compare equal; ties go to the lowest v.  Inputs must be finite.
  * d_base, d_bias: [rows, V] bf16 with row strides ld_base, ld_bias >= V.
  * d_blk: [N, B] int64, rows == N*(B-1), B >= 2, N >= 0 (N == 0 is a no-op).
- * V in [1, 2^31 - 1].  Workspace: xp_add_argmax_workspace_size(rows, V).
+ * V in [1, 2^30].  Workspace: xp_add_argmax_workspace_size(rows, V).
  * ---------------------------------------------------------------------- */
 XP_API size_t xp_add_argmax_workspace_size(int64_t rows, int64_t V);
 XP_API xp_status xp_add_argmax(const xp_bf16* d_base, int64_t ld_base, const xp_bf16* d_bias,
@@ -138,8 +138,10 @@ XP_API xp_status xp_add_argmax_noalloc(const xp_bf16* d_base, int64_t ld_base, c
  * d_blk [N,B] int64, d_am1 [N] int64, d_hcache [N,B,R] bf16, d_E [V,D] bf16,
  * d_W_lat [D,R] bf16, d_L [B,B,R] float32 (entries above the diagonal are
  * ignored), d_Wg/d_Wu [R,H] bf16, d_Wd [H,R] bf16, d_lat_out [N,B-1,R] bf16.
- * All dense (no padding).  Constraints: 2 <= B <= 16, R and D multiples of 64,
- * H a multiple of 64.  Workspace: xp_latent_workspace_size(N,B,D,R,H).
+ * All dense (no padding).  Constraints (else XP_ERR_SHAPE / XP_ERR_ALIGN):
+ * 2 <= B <= 16; 16 <= R <= 512 with R a multiple of 16; D a multiple of 8 in
+ * [8, 2^20]; H a multiple of 64 in [64, 2^16]; N*B <= 2^22; V <= 2^30.
+ * Workspace: xp_latent_workspace_size(N,B,D,R,H).
  * ---------------------------------------------------------------------- */
 XP_API size_t xp_latent_workspace_size(int64_t N, int64_t B, int64_t D, int64_t R, int64_t H);
 XP_API xp_status xp_latent_pass(const int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_hcache,
