@@ -100,7 +100,7 @@ __device__ __forceinline__ void ro_chunk(const uint32_t (&r)[32], const uint32_t
 
 __global__ void __launch_bounds__(RO_THREADS, 1)
 readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ CUtensorMap mapBase,
-                      const ReadoutParams p) {
+                      const __grid_constant__ CUtensorMap mapLat, const ReadoutParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sB = smem;                                                  // stages x 16 KB
@@ -114,7 +114,9 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* a_ready = acc_empty + 2;
   uint64_t* drain = a_ready + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* a_full = drain + 1;  // [2]: latent rounds landed in the base ring
+  uint64_t* a_free = a_full + 2;  // the epilogue warps copied a round to TMEM
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(a_free + 1);
   __shared__ int s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -139,6 +141,9 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
     }
     mbar_init(a_ready, RO_EPI_WARPS);
     mbar_init(drain, 1);
+    mbar_init(&a_full[0], 1);
+    mbar_init(&a_full[1], 1);
+    mbar_init(a_free, RO_EPI_WARPS);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -181,22 +186,51 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
     if (dead && lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
   } else if (warp == RO_WARP_BASE) {
     // ---------------- TMA producer: base tiles (two lanes, one box each) ----------------
-    if (lane == 0) prefetch_tensormap(&mapBase);
-    for (int t = 0; t < ntiles; ++t) {
-      const int n0 = (n_begin + t) * RO_BN;
-      const uint32_t bb = t % RO_NBASE, k = t / RO_NBASE;
+    // The latent tile (A) goes first, through the still-empty base ring:
+    // rounds of up to four 64-column boxes (64 KB), each copied to TMEM by
+    // the epilogue warps before the ring is reused.
+    const int rounds = (p.kch + 3) / 4;
+    bool a_dead = false;
+    if (lane == 0) prefetch_tensormap(&mapLat);
+    for (int r = 0; r < rounds && !a_dead; ++r) {
+      const int nbox = p.kch - 4 * r < 4 ? p.kch - 4 * r : 4;
       int ok = 1;
       if (lane == 0) {
-        if (k >= 1 && !mbar_wait(&base_empty[bb], (k - 1) & 1)) ok = 0;
-        else mbar_arrive_expect_tx(&base_full[bb], RO_BASE_TILE);
+        if (r >= 1 && !mbar_wait(a_free, (r - 1) & 1)) ok = 0;
+        else mbar_arrive_expect_tx(&a_full[r], (uint32_t)nbox * RO_BASE_BOX);
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) {
-        if (lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+        a_dead = true;
         break;
       }
-      if (lane < 2)
-        tma_load_2d(sBase + (size_t)bb * RO_BASE_TILE + lane * RO_BASE_BOX, &mapBase, n0 + lane * 64,
-                    m_tile * RO_BM, &base_full[bb]);
+      if (lane < nbox)
+        tma_load_2d(sBase + (size_t)lane * RO_BASE_BOX, &mapLat, (4 * r + lane) * 64, m_tile * RO_BM, &a_full[r]);
+    }
+    {
+      int ok = 1;
+      if (lane == 0 && (a_dead || !mbar_wait(a_free, (rounds - 1) & 1))) ok = 0;
+      a_dead = !__shfl_sync(0xffffffffu, ok, 0);
+    }
+    if (a_dead) {
+      if (lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+    } else {
+      if (lane == 0) prefetch_tensormap(&mapBase);
+      for (int t = 0; t < ntiles; ++t) {
+        const int n0 = (n_begin + t) * RO_BN;
+        const uint32_t bb = t % RO_NBASE, k = t / RO_NBASE;
+        int ok = 1;
+        if (lane == 0) {
+          if (k >= 1 && !mbar_wait(&base_empty[bb], (k - 1) & 1)) ok = 0;
+          else mbar_arrive_expect_tx(&base_full[bb], RO_BASE_TILE);
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          if (lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+          break;
+        }
+        if (lane < 2)
+          tma_load_2d(sBase + (size_t)bb * RO_BASE_TILE + lane * RO_BASE_BOX, &mapBase, n0 + lane * 64,
+                      m_tile * RO_BM, &base_full[bb]);
+      }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
@@ -250,37 +284,41 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
 
     // Stage the A operand (this row of the latent, zero-padded to 64*kch)
-    // into TMEM columns [0, 32*kch): the two warps of a lane quadrant split
-    // the K chunks, and each thread issues all of its loads before storing.
+    // into TMEM columns [0, 32*kch).  The latent arrives by TMA in the base
+    // ring, 128-byte swizzled (chunk c of row rr at (c ^ rr%8)*16), in rounds
+    // of four 64-column boxes; the two warps of a lane quadrant take two
+    // boxes each.
     {
-      const uint16_t* arow = p.lat + (int64_t)(row_ok ? row : 0) * p.R;
-      const int kc0 = h * ((p.kch + 1) >> 1);
-      const int kc1 = h == 0 ? ((p.kch + 1) >> 1) : p.kch;
-      uint4 w[4][8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int k = (kc0 + i) * 64 + j * 8;  // first element of this 16-byte piece
-          w[i][j] = make_uint4(0, 0, 0, 0);
-          if (kc0 + i < kc1 && row_ok && k < p.R) w[i][j] = *reinterpret_cast<const uint4*>(arow + k);
+      const int rounds = (p.kch + 3) / 4;
+      bool ok = true;
+      for (int r = 0; r < rounds; ++r) {
+        if (ok && !mbar_wait(&a_full[r], 0)) {
+          ok = false;
+          flag_error(p.hdr, XP_DEVERR_TIMEOUT);
         }
-      }
+        if (ok) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (kc0 + i < kc1) {
-          uint32_t v[32];
+          for (int j = 0; j < 2; ++j) {
+            const int box = 2 * h + j, kc = 4 * r + box;
+            if (kc < p.kch) {
+              const uint8_t* src = sBase + (size_t)box * RO_BASE_BOX + (size_t)rr * 128;
+              uint32_t v[32];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            v[4 * j] = w[i][j].x;
-            v[4 * j + 1] = w[i][j].y;
-            v[4 * j + 2] = w[i][j].z;
-            v[4 * j + 3] = w[i][j].w;
+              for (int c = 0; c < 8; ++c) {
+                const uint4 x = *reinterpret_cast<const uint4*>(src + ((c ^ (rr & 7)) << 4));
+                v[4 * c] = x.x;
+                v[4 * c + 1] = x.y;
+                v[4 * c + 2] = x.z;
+                v[4 * c + 3] = x.w;
+              }
+              tmem_st_32x32b_x32(tmem + lane_addr + RO_TMEM_A + kc * 32, v);
+            }
           }
-          tmem_st_32x32b_x32(tmem + lane_addr + RO_TMEM_A + (kc0 + i) * 32, v);
+          tmem_st_wait();
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(a_free);  // this warp is done reading the round
       }
-      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(a_ready);
@@ -365,7 +403,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
 
 size_t readout_smem_bytes() {
   return 1024 + (size_t)RO_STAGES * RO_B_STAGE + (size_t)RO_NBASE * RO_BASE_TILE +
-         8 * (2 * RO_STAGES + 2 * RO_NBASE + 6) + 16;
+         8 * (2 * RO_STAGES + 2 * RO_NBASE + 9) + 16;
 }
 
 namespace {
@@ -413,10 +451,11 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
     info.init = true;
   }
 
-  CUtensorMap mapW2, mapBase;
+  CUtensorMap mapW2, mapBase, mapLat;
   if (!cached_map_bf16_2d(&mapW2, W2t, (uint64_t)R, (uint64_t)V, (uint64_t)R, 64, RO_BN)) return XP_ERR_LAUNCH;
   if (!cached_map_bf16_2d(&mapBase, base, (uint64_t)V, (uint64_t)rows, (uint64_t)ld_base, 64, RO_BM))
     return XP_ERR_LAUNCH;
+  if (!cached_map_bf16_2d(&mapLat, lat, (uint64_t)R, (uint64_t)rows, (uint64_t)R, 64, RO_BM)) return XP_ERR_LAUNCH;
 
   ReadoutParams p;
   ArgmaxWs w = argmax_ws(ws, rows);
@@ -436,7 +475,7 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
   p.changed = changed;
   p.keys = w.keys;
   p.hdr = w.hdr;
-  readout_argmax_kernel<<<(unsigned int)(p.mt * per), RO_THREADS, smem, stream>>>(mapW2, mapBase, p);
+  readout_argmax_kernel<<<(unsigned int)(p.mt * per), RO_THREADS, smem, stream>>>(mapW2, mapBase, mapLat, p);
   return cudaGetLastError() == cudaSuccess ? XP_OK : XP_ERR_LAUNCH;
 }
 
