@@ -71,6 +71,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     if ((it & 255u) == 255u && globaltimer() - t0 > kWaitLimitNs) return false;
   }
 }
+// mbar_wait for a barrier that other CTAs of the cluster arrive on with
+// release.cluster semantics: acquire at cluster scope
+__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_acq_cluster(a, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait_acq_cluster(a, parity)) return true;
+    if ((it & 255u) == 255u && globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 
 // 2-D tiled tensor copy through a tensor map (coordinates in elements,
 // innermost first).
@@ -98,12 +121,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
-  asm volatile("mov.u32 %0, %cluster_ctarank;" : "=r"(r));
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
 __device__ __forceinline__ uint32_t cluster_nctarank() {
   uint32_t r;
-  asm volatile("mov.u32 %0, %cluster_nctarank;" : "=r"(r));
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
 }
 // Cluster-wide barrier (every thread of every CTA of the cluster); the
@@ -161,6 +184,60 @@ __device__ __forceinline__ void cp_async_4(void* dst, const void* src, uint32_t 
 }
 // wait until every cp.async this thread issued has landed in shared memory
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// CTA pairs (a cluster of two CTAs issuing tcgen05 with .cta_group::2): the
+// even CTA ("leader") issues the MMAs, whose A rows and B columns are split
+// between the two CTAs' memories at the same addresses.  A kernel that uses
+// .cta_group::2 must use it on every tcgen05 instruction that takes it.
+// ---------------------------------------------------------------------------
+// arrive on a barrier of another CTA of the cluster (address from mapa)
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+// tensor-memory allocation in both CTAs of the pair (one warp of each CTA
+// executes it; both receive the same address)
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D[256 x N] (+)= A[256 x 16] * B[16 x N] over the pair: A rows 0..127 from
+// this CTA's TMEM and 128..255 from the peer's (same address); B columns
+// [0, N/2) from the leader's shared memory and [N/2, N) from the peer's (same
+// descriptor); each CTA's TMEM receives its 128 rows x N.
+__device__ __forceinline__ void tc_mma_f16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                   bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+// arrive on `bar` (same offset) in every CTA of cta_mask once the pair's
+// earlier MMAs have completed
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+// 2-D tiled TMA into this CTA's shared memory whose completion is counted on
+// the barrier at shared::cluster address bar_cluster (the leader's)
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
 
 // programmatic dependent launch: wait for the preceding kernel's results /
 // let the next kernel start its prologue

@@ -9,28 +9,35 @@
 // _xpress_add_argmax_partial_kernel).  The [rows, V] bias and logits never
 // reach memory.
 //
-// GB300 design (tcgen05 + TMEM + TMA):
+// GB300 design (tcgen05 + TMEM + TMA, CTA pairs):
 //   * W2 is read vocabulary-major (W2t = W2 transposed, [V, R]), so the
-//     weights of one 128-wide vocab tile are one contiguous 128 KB block of
-//     memory rather than 128-byte pieces of 512 distant rows;
-//   * one CTA per SM; CTA (m, j) owns M tile m (128 draft rows) and a
-//     contiguous range of vocab tiles;
-//   * the CTA's 128 x R slice of the latent (the MMA's A operand) is written
-//     ONCE into tensor memory (256 columns for R = 512) and every MMA reads
-//     it from there, which leaves shared memory to the streamed operands;
-//   * two producer threads (warps 0 and 10) stream W2t through a ring of
-//     4 stages of 128 vocab x 128 K (two 16 KB TMA boxes each), each owning
-//     alternate stages so their issue costs overlap; warp 11 streams the
-//     matching 128 x 128 base tile into a second ring (128-byte swizzle
-//     throughout);
-//   * warp 1 (one thread) issues tcgen05.mma M=128 N=128 K=16 (A in TMEM,
-//     B in shared memory, fp32 accumulate) into one of two 128-column TMEM
-//     accumulators, so the epilogue of tile t overlaps the MMAs of tile t+1;
+//     weights of a vocab tile are one contiguous block of memory rather than
+//     128-byte pieces of distant rows;
+//   * CTAs work in pairs (a 2-CTA cluster): the pair owns two M tiles of 128
+//     draft rows (one per CTA) and a contiguous range of 128-wide vocab tiles.
+//     The leader issues tcgen05.mma.cta_group::2 with M = 256, N = 128: each
+//     CTA holds its own 128 rows of the latent (the A operand) in tensor
+//     memory and streams only ITS 64-vocab half of every W2 tile, yet
+//     receives the full 128 x 128 accumulator for its rows.  Every W2 byte an
+//     SM ingests thus serves 256 rows instead of 128, which halves the
+//     per-SM W2 traffic, the limit of this stream;
+//   * each CTA's 128 x R latent slice is staged ONCE into tensor memory (256
+//     columns for R = 512): TMA brings it into the (still empty) base ring and
+//     the epilogue warps copy their rows into TMEM lanes;
+//   * two producer warps (0 and 10) stream the CTA's W2t half through a ring
+//     of 4 stages of 64 vocab x 256 K (four 8 KB TMA boxes, one lane each),
+//     alternate stages each; the copies complete on the leader's barrier so
+//     one wait covers both halves; warp 11 streams the CTA's 128 x 128 base
+//     tiles into a 3-deep ring (128-byte swizzle throughout);
+//   * the leader's warp 1 issues the MMAs into one of two 128-column TMEM
+//     accumulators (the epilogue of tile t overlaps the MMAs of tile t+1) and
+//     commits them to the barriers of both CTAs at once;
 //   * warps 2..9 drain the accumulator with tcgen05.ld (thread = one row,
 //     warp = a 32-lane quadrant and a 64-column half), round to bf16, add the
 //     base tile from shared memory and keep a running (max, first column)
 //     per row across the CTA's tiles (tiles and columns ascend, so a strict
-//     '>' keeps the lowest index);
+//     '>' keeps the lowest index); both CTAs' epilogues release an
+//     accumulator on the leader's barrier;
 //   * each row's per-CTA winner is folded into a 64-bit (value, lowest
 //     index) key with atomicMax; the last CTA to finish writes blk, counts the
 //     changed slots and re-zeroes the keys.
@@ -41,29 +48,30 @@
 
 namespace xp {
 
-constexpr int RO_BM = 128;
-constexpr int RO_BN = 128;
+constexpr int RO_BM = 128;                             // draft rows per CTA (M per CTA)
+constexpr int RO_BN = 128;                             // vocab per tile (N of the pair's MMA)
+constexpr int RO_HALF = RO_BN / 2;                     // vocab rows of W2t a CTA streams per tile
 constexpr int RO_EPI_WARPS = 8;
-// warp 0: W2 producer (even stages); warp 1: MMA issuer; warps 2..9:
-// epilogue; warp 10: W2 producer (odd stages); warp 11: base producer.
+// warp 0: W2 producer (even stages); warp 1: MMA issuer (leader); warps 2..9:
+// epilogue; warp 10: W2 producer (odd stages); warp 11: latent + base producer.
 constexpr int RO_WARP_W2B = 2 + RO_EPI_WARPS;
 constexpr int RO_WARP_BASE = RO_WARP_W2B + 1;
 constexpr int RO_THREADS = (RO_WARP_BASE + 1) * 32;
-constexpr int RO_KS = 128;                             // K per W2 stage
-constexpr uint32_t RO_W2_BOX = 64 * RO_BN * 2;         // 64 K x 128 vocab (16 KB)
-constexpr uint32_t RO_B_STAGE = 2 * RO_W2_BOX;         // 32 KB
-constexpr int RO_STAGES = 5;                           // stage s is always refilled by producer s % 2
+constexpr int RO_KS = 256;                             // K per W2 stage
+constexpr uint32_t RO_W2_BOX = 64 * RO_HALF * 2;       // 64 K x 64 vocab (8 KB)
+constexpr uint32_t RO_B_STAGE = (RO_KS / 64) * RO_W2_BOX;  // 32 KB per CTA
+constexpr int RO_STAGES = 4;                           // stage s is always refilled by producer s % 2
 constexpr uint32_t RO_BASE_BOX = RO_BM * 64 * 2;       // base box: 128 rows x 64 cols (16 KB)
 constexpr uint32_t RO_BASE_TILE = RO_BM * RO_BN * 2;   // 32 KB
-constexpr int RO_NBASE = 2;
+constexpr int RO_NBASE = 3;
 constexpr int RO_MAX_KCH = 8;                          // R <= 512 (K chunks of 64 in TMEM)
 constexpr uint32_t RO_TMEM_A = 0;                      // A: columns [0, 32*kch)
 constexpr uint32_t RO_TMEM_ACC = 256;                  // accumulators: [256, 384), [384, 512)
 
 struct ReadoutParams {
   const uint16_t* lat;
-  int32_t rows, V, R, kch, mt, nt, per, B;
-  int32_t nks;      // W2 stages per tile: ceil(R / 128); kch = 2 * nks
+  int32_t rows, V, R, kch, mp, nt, per, B;
+  int32_t nks;      // W2 stages per tile: ceil(R / 256); kch = 4 * nks
   int64_t* blk;
   int32_t* changed;
   unsigned long long* keys;
@@ -120,16 +128,21 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   __shared__ int s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_tile = (int)(blockIdx.x % p.mt);
-  const int jslot = (int)(blockIdx.x / p.mt);
+  const uint32_t rank = cluster_ctarank();  // 0: the pair's leader
+  const int pair = (int)(blockIdx.x >> 1);
+  const int m_tile = 2 * (pair % p.mp) + (int)rank;
+  const int jslot = pair / p.mp;
   const int n_begin = (int)((int64_t)jslot * p.nt / p.per);
   const int n_end = (int)((int64_t)(jslot + 1) * p.nt / p.per);
   const int ntiles = n_end - n_begin;
 
+  // Barriers live at the same offsets in both CTAs.  b_full, acc_empty and
+  // a_ready are used in the leader only (both CTAs count on them); b_empty
+  // and acc_full are arrived on in both CTAs by the leader's commits.
   if (threadIdx.x == 0) {
     for (int s = 0; s < RO_STAGES; ++s) {
-      mbar_init(&b_full[s], 1);   // the owning W2 producer's arrive_expect_tx
-      mbar_init(&b_empty[s], 1);  // the MMA's release
+      mbar_init(&b_full[s], 1);   // the leader's arrive_expect_tx (both halves' bytes)
+      mbar_init(&b_empty[s], 1);  // the pair's MMAs released the stage
     }
     for (int s = 0; s < RO_NBASE; ++s) {
       mbar_init(&base_full[s], 1);
@@ -137,9 +150,9 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], RO_EPI_WARPS);
+      mbar_init(&acc_empty[a], 2 * RO_EPI_WARPS);
     }
-    mbar_init(a_ready, RO_EPI_WARPS);
+    mbar_init(a_ready, 2 * RO_EPI_WARPS);
     mbar_init(drain, 1);
     mbar_init(&a_full[0], 1);
     mbar_init(&a_full[1], 1);
@@ -147,20 +160,29 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, 512);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any cross-CTA arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the leader's copy of a barrier, as a shared::cluster address
+  auto leader_bar = [](uint64_t* b) { return mapa_shared(smem_u32(b), 0u); };
+  // arrive on the leader's copy of a barrier (locally in the leader)
+  auto arrive_leader = [&](uint64_t* b) {
+    if (rank == 0) mbar_arrive(b);
+    else mbar_arrive_remote(leader_bar(b));
+  };
 
   if (warp == 0 || warp == RO_WARP_W2B) {
     // ---------------- TMA producers: W2t stages ----------------
     // stage s is always refilled by producer s % 2, so each producer's waits
     // on a stage follow that stage's uses in order.  Lane 0 waits for the
-    // stage and arms its barrier; lanes 0 and 1 issue one box each (a single
-    // thread issues tiled copies slowly)
+    // stage (and, in the leader, arms the pair's barrier for both halves);
+    // lanes 0..3 issue one box each (a single thread issues tiled copies
+    // slowly)
     const uint32_t pid = warp == 0 ? 0u : 1u;
     if (pid == 0 && lane == 0) prefetch_tensormap(&mapW2);
     uint32_t it = 0;
@@ -173,14 +195,16 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
         int ok = 1;
         if (lane == 0) {
           if (k >= 1 && !mbar_wait(&b_empty[s], (k - 1) & 1)) ok = 0;
-          else mbar_arrive_expect_tx(&b_full[s], RO_B_STAGE);
+          else if (rank == 0) mbar_arrive_expect_tx(&b_full[s], 2 * RO_B_STAGE);
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
           dead = true;
           break;
         }
-        if (lane < 2) tma_load_2d(sB + (size_t)s * RO_B_STAGE + lane * RO_W2_BOX, &mapW2, ks * RO_KS + lane * 64, n0,
-                                  &b_full[s]);
+        // this CTA's half: vocab rows [n0 + 64 * rank, +64) of W2t
+        if (lane < RO_KS / 64)
+          tma_load_2d_pair(sB + (size_t)s * RO_B_STAGE + lane * RO_W2_BOX, &mapW2, ks * RO_KS + lane * 64,
+                           n0 + (int)rank * RO_HALF, leader_bar(&b_full[s]));
       }
     }
     if (dead && lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
@@ -233,15 +257,15 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(RO_BM, RO_BN, 0, 0);
-      bool dead = !mbar_wait(a_ready, 0);
+    // ---------------- MMA issuer (the pair's leader) ----------------
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * RO_BM, RO_BN, 0, 0);
+      bool dead = !mbar_wait_cluster(a_ready, 0);
       tc_fence_after();
       uint32_t it = 0;
       for (int t = 0; t < ntiles && !dead; ++t) {
         const uint32_t a = t & 1, u = t >> 1;
-        if (u >= 1 && !mbar_wait(&acc_empty[a], (u - 1) & 1)) {
+        if (u >= 1 && !mbar_wait_cluster(&acc_empty[a], (u - 1) & 1)) {
           dead = true;
           break;
         }
@@ -263,15 +287,15 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
             // B: K-major (W2t rows), 128-byte rows, 8-row groups 1024 B apart;
             // a K step of 16 advances 32 bytes inside a 64-wide box.
             const uint64_t bdesc = smem_desc_sw128(b_base + (kk >> 2) * RO_W2_BOX + (kk & 3) * 32, 16, 1024);
-            tc_mma_f16_ts(d, a_tm, bdesc, idesc, (ks | kk) != 0);
+            tc_mma_f16_ts_pair(d, a_tm, bdesc, idesc, (ks | kk) != 0);
           }
-          tc_commit(&b_empty[s]);
+          tc_commit_pair(&b_empty[s], 0x3);
         }
         if (dead) break;
-        tc_commit(&acc_full[a]);
+        tc_commit_pair(&acc_full[a], 0x3);
       }
       if (dead) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
-      tc_commit(drain);
+      tc_commit_pair(drain, 0x1);
       (void)mbar_wait(drain, 0);
     }
   } else if (warp >= 2 && warp < 2 + RO_EPI_WARPS) {
@@ -321,7 +345,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(a_ready);
+      if (lane == 0) arrive_leader(a_ready);
     }
 
     float best = -INFINITY;
@@ -361,7 +385,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&acc_empty[a]);
+        arrive_leader(&acc_empty[a]);
         mbar_arrive(&base_empty[bb]);
       }
     }
@@ -372,10 +396,13 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   __syncwarp();  // lane-0 roles rejoin their warps before any .aligned op
   tc_fence_before();
   __syncthreads();
+  // the leader's MMAs are complete (drain) and no remote arrive is in flight
+  // once both CTAs are here
+  cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc_pair(tmem, 512);
   }
   if (threadIdx.x == 0) {
     __threadfence();
@@ -407,16 +434,17 @@ size_t readout_smem_bytes() {
 }
 
 namespace {
-// Work split: mt M tiles of 128 rows x per contiguous vocabulary ranges of
-// 128-wide tiles, one CTA each (mt * per <= SMs).
+// Work split: mp pairs of 128-row M tiles x per contiguous vocabulary ranges
+// of 128-wide tiles, one CTA pair each (2 * mp * per <= SMs).
 struct RoSplit {
-  int32_t mt, nt, per;
+  int32_t mp, nt, per;
 };
 RoSplit readout_split(int sms, int64_t rows, int64_t V) {
   RoSplit s;
-  s.mt = (int32_t)((rows + RO_BM - 1) / RO_BM);
+  const int64_t mt = (rows + RO_BM - 1) / RO_BM;
+  s.mp = (int32_t)((mt + 1) / 2);
   s.nt = (int32_t)((V + RO_BN - 1) / RO_BN);
-  s.per = sms / s.mt;
+  s.per = sms / (2 * s.mp);
   if (s.per < 1) s.per = 1;
   if (s.per > s.nt) s.per = s.nt;
   return s;
@@ -434,7 +462,7 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
                                 void* ws, cudaStream_t stream) {
   if (rows <= 0) return XP_OK;
   const int nks = (int)((R + RO_KS - 1) / RO_KS);
-  if (2 * nks > RO_MAX_KCH) return XP_ERR_SHAPE;
+  if (4 * nks > RO_MAX_KCH) return XP_ERR_SHAPE;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return XP_ERR_LAUNCH;
   RoDevInfo& info = g_ro_dev[dev];
@@ -452,7 +480,7 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
   }
 
   CUtensorMap mapW2, mapBase, mapLat;
-  if (!cached_map_bf16_2d(&mapW2, W2t, (uint64_t)R, (uint64_t)V, (uint64_t)R, 64, RO_BN)) return XP_ERR_LAUNCH;
+  if (!cached_map_bf16_2d(&mapW2, W2t, (uint64_t)R, (uint64_t)V, (uint64_t)R, 64, RO_HALF)) return XP_ERR_LAUNCH;
   if (!cached_map_bf16_2d(&mapBase, base, (uint64_t)V, (uint64_t)rows, (uint64_t)ld_base, 64, RO_BM))
     return XP_ERR_LAUNCH;
   if (!cached_map_bf16_2d(&mapLat, lat, (uint64_t)R, (uint64_t)rows, (uint64_t)R, 64, RO_BM)) return XP_ERR_LAUNCH;
@@ -465,8 +493,8 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
   p.V = (int32_t)V;
   p.R = (int32_t)R;
   p.nks = nks;
-  p.kch = 2 * nks;  // A staged in TMEM up to the last W2 stage, zero beyond R
-  p.mt = sp.mt;
+  p.kch = 4 * nks;  // A staged in TMEM up to the last W2 stage, zero beyond R
+  p.mp = sp.mp;
   p.nt = sp.nt;
   p.per = sp.per;
   const int per = sp.per;
@@ -475,7 +503,19 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
   p.changed = changed;
   p.keys = w.keys;
   p.hdr = w.hdr;
-  readout_argmax_kernel<<<(unsigned int)(p.mt * per), RO_THREADS, smem, stream>>>(mapW2, mapBase, mapLat, p);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned int)(2 * p.mp * per));
+  cfg.blockDim = dim3(RO_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, readout_argmax_kernel, mapW2, mapBase, mapLat, p) != cudaSuccess) return XP_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? XP_OK : XP_ERR_LAUNCH;
 }
 
