@@ -96,7 +96,7 @@ def traffic_from_profile():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -110,7 +110,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                          "-lms", "100", "-i", str(self.index)], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -124,8 +124,11 @@ class ClockSampler:
             if len(parts) >= 9:
                 self.samples.append((time.time(), parts))
 
-    def mark(self):
-        return time.time()
+    def wait_first(self, limit_s: float = 5.0):
+        """Block until nvidia-smi has printed its first sample (or the limit)."""
+        t_end = time.time() + limit_s
+        while self.proc and not self.samples and time.time() < t_end:
+            time.sleep(0.05)
 
     def __exit__(self, *a):
         if self.proc:
@@ -264,8 +267,18 @@ def run_gb300(args, rank, world, local_rank):
 
     # ---- the timed passes
     with ClockSampler(local_rank) as clk:
+        clk.wait_first()
         for i in range(args.warmup):
             step(i)
+        # keep the GPU under the same load for ~0.6 s more (untimed), so that
+        # the 100 ms clock samples around the short timed region see it loaded
+        t_soak = time.time() + 0.6
+        i = args.warmup
+        while time.time() < t_soak:
+            for _ in range(64):
+                step(i)
+                i += 1
+            torch.cuda.synchronize()
         reset()
         torch.cuda.synchronize()
         if world > 1:

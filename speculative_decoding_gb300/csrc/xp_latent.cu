@@ -29,6 +29,7 @@
 #include "xp_internal.h"
 #include "xp_ptx.cuh"
 #include "xp_tma.cuh"
+#include "xp_trace.cuh"
 
 namespace xp {
 
@@ -75,6 +76,7 @@ __host__ __device__ inline uint32_t proj_ls_bytes(int B, int w) {
 __global__ void __launch_bounds__(LT_THREADS, 2)
 proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p) {
   extern __shared__ uint8_t smem_raw[];
+  if (threadIdx.x == 0) XP_TRACE_MARK(0);
   uint8_t* smem = align1024(smem_raw);
   const uint32_t b_bytes = (uint32_t)p.tn * LT_BK * 2;
   const uint32_t stage_bytes = LT_A_CHUNK + b_bytes;
@@ -114,8 +116,10 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) XP_TRACE_MARK(1);
   pdl_launch_dependents();
   pdl_wait();  // blk may have been written by the preceding pass
+  if (threadIdx.x == 0) XP_TRACE_MARK(2);
 
   if (warp == 0) {
     // lane 0 waits for the stage and arms its barrier; lanes 0..tn/64-1 then
@@ -127,6 +131,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
       if (lane == 0) {
         if (k >= 1 && !mbar_wait(&empty[s], (k - 1) & 1)) ok = 0;
         else mbar_arrive_expect_tx(&full[s], b_bytes);
+        if (k >= 1 && i - p.stages < 8) XP_TRACE_MARK(48 + i - p.stages);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
@@ -137,6 +142,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
         tma_load_2d(smem + (size_t)s * stage_bytes + LT_A_CHUNK + lane * LT_BOX, &mapWlat, nt * p.tn + lane * 64,
                     (c0 + i) * LT_BK, &full[s]);
     }
+    if (lane == 0) XP_TRACE_MARK(3);
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(LT_BM, p.tn, 0, 1);
@@ -148,6 +154,8 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
           break;
         }
         tc_fence_after();
+        if (i == 0) XP_TRACE_MARK(7);
+        if (i < 7) XP_TRACE_MARK(56 + i);
         const uint32_t a_base = smem_u32(smem + (size_t)s * stage_bytes);
         const uint32_t b_base = a_base + LT_A_CHUNK;
 #pragma unroll
@@ -160,6 +168,10 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
       }
       if (dead) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
       tc_commit(acc_full);
+      XP_TRACE_MARK(8);
+#ifdef XP_TRACE
+      if (mbar_wait(acc_full, 0)) XP_TRACE_MARK(15);
+#endif
     }
   } else {
     const int et = threadIdx.x - 64;  // 0..127
@@ -177,6 +189,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
       tok[et] = t;
     }
     named_barrier_sync(1, 128);
+    if (threadIdx.x == 64) XP_TRACE_MARK(4);
     // gather: warp gw owns the stages s with s % 4 == gw and refills them in
     // order.  Eight lanes cover one 128-byte row piece, so each copy
     // instruction reads four whole rows; cp.async keeps all 32 copies of a
@@ -204,6 +217,8 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[s]);
+      if (lane == 0 && i == 0) XP_TRACE_MARK(5);
+      if (lane == 0 && i == nck - 1) XP_TRACE_MARK(6);
     }
     // the mixer weights of this CTA's columns, copied in the background while
     // the MMAs finish (waited for before the mixer)
@@ -222,6 +237,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
   if (warp >= 2) {
     if (!mbar_wait(acc_full, 0)) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
     tc_fence_after();
+    if (threadIdx.x == 64) XP_TRACE_MARK(9);
     const int q = warp & 3, row = q * 32 + lane;
     for (int c = 0; c < p.tn / 32; ++c) {
       uint32_t r[32];
@@ -234,11 +250,13 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
                              __uint_as_float(r[4 * e + 3]));
     }
   }
+  if (threadIdx.x == 64) XP_TRACE_MARK(10);
   tc_fence_before();
   cluster_sync();
 
   if (warp >= 2) {
     const int et = threadIdx.x - 64;
+    if (et == 0) XP_TRACE_MARK(11);
     // ---- epilogue 2: x = hcache + sum of the cluster's partials (fixed
     // order) for this CTA's columns of all rows; two (row, 4 columns) items
     // per thread per round, every partial requested before any is used
@@ -285,6 +303,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
         *reinterpret_cast<float4*>(xs + rr[h] * p.w + 4 * gg[h]) = x;
       }
     }
+    if (et == 0) XP_TRACE_MARK(12);
     cp_async_wait_all();  // this thread's share of Ls
     named_barrier_sync(1, 128);
     // ---- the causal mixer on this CTA's columns: u[b] = sum_{j<=b} L[b,j] x[j]
@@ -309,8 +328,10 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
         }
       }
     }
+    if (et == 0) XP_TRACE_MARK(13);
   }
   cluster_sync();  // the peers have finished reading this CTA's partial sums
+  if (threadIdx.x == 0) XP_TRACE_MARK(14);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 128);
@@ -330,6 +351,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
 mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__ CUtensorMap mapWg,
               const __grid_constant__ CUtensorMap mapWu, const UpParams p) {
   extern __shared__ uint8_t smem_raw[];
+  if (threadIdx.x == 0) XP_TRACE_MARK(16);
   uint8_t* smem = align1024(smem_raw);
   constexpr uint32_t stage_bytes = LT_A_CHUNK + 2 * LT_BOX;  // 32 KB
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)p.stages * stage_bytes);
@@ -357,8 +379,10 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) XP_TRACE_MARK(17);
   pdl_launch_dependents();
   pdl_wait();  // ub comes from proj_mix
+  if (threadIdx.x == 0) XP_TRACE_MARK(18);
 
   if (warp == 0) {
     // lane 0 arms the stage; lanes 0, 1, 2 issue the ub, Wg and Wu boxes
@@ -395,6 +419,7 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
           break;
         }
         tc_fence_after();
+        if (i == 0) XP_TRACE_MARK(19);
         const uint32_t a_base = smem_u32(smem + (size_t)s * stage_bytes);
 #pragma unroll
         for (int kk = 0; kk < LT_BK / 16; ++kk) {
@@ -408,10 +433,12 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
       }
       if (dead) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
       tc_commit(acc_full);
+      XP_TRACE_MARK(20);
     }
   } else {
     if (!mbar_wait(acc_full, 0)) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
     tc_fence_after();
+    if (threadIdx.x == 64) XP_TRACE_MARK(21);
     const int q = warp & 3;
     const int row = mt * LT_BM + q * 32 + lane;
 #pragma unroll
@@ -434,6 +461,7 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
         for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
       }
     }
+    if (threadIdx.x == 64) XP_TRACE_MARK(22);
   }
   tc_fence_before();
   __syncthreads();
@@ -460,6 +488,7 @@ __global__ void __launch_bounds__(LT_THREADS, 2)
 mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant__ CUtensorMap mapWd,
                 const DownParams p) {
   extern __shared__ uint8_t smem_raw[];
+  if (threadIdx.x == 0) XP_TRACE_MARK(32);
   uint8_t* smem = align1024(smem_raw);
   const uint32_t b_bytes = (uint32_t)p.tn * LT_BK * 2;
   const uint32_t stage_bytes = LT_A_CHUNK + b_bytes;
@@ -496,8 +525,10 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) XP_TRACE_MARK(33);
   pdl_launch_dependents();
   pdl_wait();  // m comes from mlp_up
+  if (threadIdx.x == 0) XP_TRACE_MARK(34);
 
   if (warp == 0) {
     // lane 0 arms the stage; lane 0 issues the m box, lanes 1.. the Wd boxes
@@ -534,6 +565,7 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
           break;
         }
         tc_fence_after();
+        if (i == 0) XP_TRACE_MARK(32 + 7);
         const uint32_t a_base = smem_u32(smem + (size_t)s * stage_bytes);
         const uint32_t b_base = a_base + LT_A_CHUNK;
 #pragma unroll
@@ -546,10 +578,12 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
       }
       if (dead) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
       tc_commit(acc_full);
+      XP_TRACE_MARK(32 + 8);
     }
   } else {
     if (!mbar_wait(acc_full, 0)) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
     tc_fence_after();
+    if (threadIdx.x == 64) XP_TRACE_MARK(41);
     const int q = warp & 3, row = q * 32 + lane;
     for (int c = 0; c < p.tn / 32; ++c) {
       uint32_t r[32];
@@ -562,8 +596,10 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
                              __uint_as_float(r[4 * e + 3]));
     }
   }
+  if (threadIdx.x == 64) XP_TRACE_MARK(42);
   tc_fence_before();
   cluster_sync();
+  if (threadIdx.x == 64) XP_TRACE_MARK(43);
 
   // ---- sum the cluster's partials for this CTA's columns (fixed order), add
   // the residual u, write slots 1..B-1.  Two (row, 4 columns) items per
@@ -608,8 +644,10 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
             make_uint2(f32x2_to_bf16x2(uu[h].x + a.x, uu[h].y + a.y), f32x2_to_bf16x2(uu[h].z + a.z, uu[h].w + a.w));
       }
     }
+    if (et == 0) XP_TRACE_MARK(44);
   }
   cluster_sync();
+  if (threadIdx.x == 0) XP_TRACE_MARK(45);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 128);
@@ -809,3 +847,5 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
 }
 
 }  // namespace xp
+
+XP_TRACE_READER(xp_trace_read_latent)

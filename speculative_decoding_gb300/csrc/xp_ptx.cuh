@@ -59,6 +59,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a waiting thread sleeps in hardware
+// until the phase completes (or the hint's time passes) instead of spinning
+// and taking issue slots from the warps that do the work.
+constexpr uint32_t kSuspendHintNs = 20000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed.  Returns false if
 // the wall-clock limit passed first (the caller records the timeout and
 // stops).
@@ -66,9 +82,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const unsigned long long t0 = globaltimer();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(a, parity)) return true;
-    if ((it & 255u) == 255u && globaltimer() - t0 > kWaitLimitNs) return false;
+  for (;;) {
+    if (mbar_try_wait_sleep(a, parity)) return true;
+    if (globaltimer() - t0 > kWaitLimitNs) return false;
   }
 }
 // mbar_wait for a barrier that other CTAs of the cluster arrive on with
@@ -84,13 +100,24 @@ __device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t bar_addr, uin
       : "memory");
   return ok != 0;
 }
+__device__ __forceinline__ bool mbar_try_wait_acq_cluster_sleep(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait_acq_cluster(a, parity)) return true;
   const unsigned long long t0 = globaltimer();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait_acq_cluster(a, parity)) return true;
-    if ((it & 255u) == 255u && globaltimer() - t0 > kWaitLimitNs) return false;
+  for (;;) {
+    if (mbar_try_wait_acq_cluster_sleep(a, parity)) return true;
+    if (globaltimer() - t0 > kWaitLimitNs) return false;
   }
 }
 

@@ -24,14 +24,17 @@
 //   * each CTA's 128 x R latent slice is staged ONCE into tensor memory (256
 //     columns for R = 512): TMA brings it into the (still empty) base ring and
 //     the epilogue warps copy their rows into TMEM lanes;
-//   * two producer warps (0 and 10) stream the CTA's W2t half through a ring
-//     of 4 stages of 64 vocab x 256 K (four 8 KB TMA boxes, one lane each),
-//     alternate stages each; the copies complete on the leader's barrier so
-//     one wait covers both halves; warp 11 streams the CTA's 128 x 128 base
-//     tiles into a 3-deep ring (128-byte swizzle throughout);
-//   * the leader's warp 1 issues the MMAs into one of two 128-column TMEM
-//     accumulators (the epilogue of tile t overlaps the MMAs of tile t+1) and
-//     commits them to the barriers of both CTAs at once;
+//   * the W2t half-tiles (64 vocab x R, up to eight 8 KB TMA boxes, one lane
+//     each) go into two tile slots, refilled by two producer warps (0 and 10,
+//     one slot each); the copies of both CTAs complete on the leader's
+//     barrier, so one wait covers both halves; warp 11 streams the CTA's
+//     128 x 128 base tiles into a 3-deep ring (128-byte swizzle throughout);
+//   * the leader's warp 1 issues the MMAs of tile t into accumulator t % 2
+//     (two 128-column TMEM accumulators: the epilogue of tile t overlaps the
+//     MMAs of tile t+1) and commits them ONCE per tile to the barriers of
+//     both CTAs: that commit both hands the accumulator to the epilogue and
+//     frees the W2 slot of tile t for tile t+2 (a pair's commit is costly, so
+//     there is no separate per-stage release);
 //   * warps 2..9 drain the accumulator with tcgen05.ld (thread = one row,
 //     warp = a 32-lane quadrant and a 64-column half), round to bf16, add the
 //     base tile from shared memory and keep a running (max, first column)
@@ -45,6 +48,7 @@
 #include "xp_internal.h"
 #include "xp_ptx.cuh"
 #include "xp_tma.cuh"
+#include "xp_trace.cuh"
 
 namespace xp {
 
@@ -57,21 +61,19 @@ constexpr int RO_EPI_WARPS = 8;
 constexpr int RO_WARP_W2B = 2 + RO_EPI_WARPS;
 constexpr int RO_WARP_BASE = RO_WARP_W2B + 1;
 constexpr int RO_THREADS = (RO_WARP_BASE + 1) * 32;
-constexpr int RO_KS = 256;                             // K per W2 stage
 constexpr uint32_t RO_W2_BOX = 64 * RO_HALF * 2;       // 64 K x 64 vocab (8 KB)
-constexpr uint32_t RO_B_STAGE = (RO_KS / 64) * RO_W2_BOX;  // 32 KB per CTA
-constexpr int RO_STAGES = 4;                           // stage s is always refilled by producer s % 2
+constexpr int RO_MAX_KCH = 8;                          // R <= 512 (K chunks of 64)
+constexpr uint32_t RO_W2_SLOT = RO_MAX_KCH * RO_W2_BOX;  // one tile's W2t half: 64 KB per CTA
+constexpr int RO_SLOTS = 2;                            // slot t % 2 holds tile t, refilled by producer t % 2
 constexpr uint32_t RO_BASE_BOX = RO_BM * 64 * 2;       // base box: 128 rows x 64 cols (16 KB)
 constexpr uint32_t RO_BASE_TILE = RO_BM * RO_BN * 2;   // 32 KB
 constexpr int RO_NBASE = 3;
-constexpr int RO_MAX_KCH = 8;                          // R <= 512 (K chunks of 64 in TMEM)
 constexpr uint32_t RO_TMEM_A = 0;                      // A: columns [0, 32*kch)
 constexpr uint32_t RO_TMEM_ACC = 256;                  // accumulators: [256, 384), [384, 512)
 
 struct ReadoutParams {
   const uint16_t* lat;
-  int32_t rows, V, R, kch, mp, nt, per, B;
-  int32_t nks;      // W2 stages per tile: ceil(R / 256); kch = 4 * nks
+  int32_t rows, V, R, kch, mp, nt, per, B;  // kch = ceil(R / 64) K chunks (boxes) per tile
   int64_t* blk;
   int32_t* changed;
   unsigned long long* keys;
@@ -111,12 +113,11 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
                       const __grid_constant__ CUtensorMap mapLat, const ReadoutParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sB = smem;                                                  // stages x 16 KB
-  uint8_t* sBase = smem + (size_t)RO_STAGES * RO_B_STAGE;               // RO_NBASE x 32 KB
+  uint8_t* sB = smem;                                                  // RO_SLOTS x 64 KB
+  uint8_t* sBase = smem + (size_t)RO_SLOTS * RO_W2_SLOT;                // RO_NBASE x 32 KB
   uint64_t* bars = reinterpret_cast<uint64_t*>(sBase + (size_t)RO_NBASE * RO_BASE_TILE);
   uint64_t* b_full = bars;
-  uint64_t* b_empty = b_full + RO_STAGES;
-  uint64_t* base_full = b_empty + RO_STAGES;
+  uint64_t* base_full = b_full + RO_SLOTS;
   uint64_t* base_empty = base_full + RO_NBASE;
   uint64_t* acc_full = base_empty + RO_NBASE;
   uint64_t* acc_empty = acc_full + 2;
@@ -126,6 +127,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   uint64_t* a_free = a_full + 2;  // the epilogue warps copied a round to TMEM
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(a_free + 1);
   __shared__ int s_last;
+  if (threadIdx.x == 0) XP_TRACE_MARK(0);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: the pair's leader
@@ -137,13 +139,10 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   const int ntiles = n_end - n_begin;
 
   // Barriers live at the same offsets in both CTAs.  b_full, acc_empty and
-  // a_ready are used in the leader only (both CTAs count on them); b_empty
-  // and acc_full are arrived on in both CTAs by the leader's commits.
+  // a_ready are used in the leader only (both CTAs count on them); acc_full
+  // is arrived on in both CTAs by the leader's commits.
   if (threadIdx.x == 0) {
-    for (int s = 0; s < RO_STAGES; ++s) {
-      mbar_init(&b_full[s], 1);   // the leader's arrive_expect_tx (both halves' bytes)
-      mbar_init(&b_empty[s], 1);  // the pair's MMAs released the stage
-    }
+    for (int s = 0; s < RO_SLOTS; ++s) mbar_init(&b_full[s], 1);  // the leader's arrive_expect_tx (both halves)
     for (int s = 0; s < RO_NBASE; ++s) {
       mbar_init(&base_full[s], 1);
       mbar_init(&base_empty[s], RO_EPI_WARPS);
@@ -168,6 +167,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   cluster_sync();  // both CTAs' barriers exist before any cross-CTA arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) XP_TRACE_MARK(1);
   // the leader's copy of a barrier, as a shared::cluster address
   auto leader_bar = [](uint64_t* b) { return mapa_shared(smem_u32(b), 0u); };
   // arrive on the leader's copy of a barrier (locally in the leader)
@@ -177,37 +177,34 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   };
 
   if (warp == 0 || warp == RO_WARP_W2B) {
-    // ---------------- TMA producers: W2t stages ----------------
-    // stage s is always refilled by producer s % 2, so each producer's waits
-    // on a stage follow that stage's uses in order.  Lane 0 waits for the
-    // stage (and, in the leader, arms the pair's barrier for both halves);
-    // lanes 0..3 issue one box each (a single thread issues tiled copies
-    // slowly)
-    const uint32_t pid = warp == 0 ? 0u : 1u;
+    // ---------------- TMA producers: W2t tile slots ----------------
+    // slot s = t % 2 is always refilled by producer s, after the pair's
+    // commit of tile t-2 (acc_full of that slot, arrived in both CTAs) shows
+    // the MMAs that read it are done.  Lane 0 waits (and, in the leader,
+    // arms the pair's barrier for both halves); lanes 0..kch-1 issue one box
+    // each (a single thread issues tiled copies slowly).
+    const int pid = warp == 0 ? 0 : 1;
     if (pid == 0 && lane == 0) prefetch_tensormap(&mapW2);
-    uint32_t it = 0;
     bool dead = false;
-    for (int t = 0; t < ntiles && !dead; ++t) {
+    for (int t = pid; t < ntiles; t += RO_SLOTS) {
       const int n0 = (n_begin + t) * RO_BN;
-      for (int ks = 0; ks < p.nks; ++ks, ++it) {
-        const uint32_t s = it % RO_STAGES, k = it / RO_STAGES;
-        if ((s & 1u) != pid) continue;
-        int ok = 1;
-        if (lane == 0) {
-          if (k >= 1 && !mbar_wait(&b_empty[s], (k - 1) & 1)) ok = 0;
-          else if (rank == 0) mbar_arrive_expect_tx(&b_full[s], 2 * RO_B_STAGE);
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) {
-          dead = true;
-          break;
-        }
-        // this CTA's half: vocab rows [n0 + 64 * rank, +64) of W2t
-        if (lane < RO_KS / 64)
-          tma_load_2d_pair(sB + (size_t)s * RO_B_STAGE + lane * RO_W2_BOX, &mapW2, ks * RO_KS + lane * 64,
-                           n0 + (int)rank * RO_HALF, leader_bar(&b_full[s]));
+      const uint32_t u = (uint32_t)t >> 1;
+      int ok = 1;
+      if (lane == 0) {
+        if (u >= 1 && !mbar_wait_cluster(&acc_full[pid], (u - 1) & 1)) ok = 0;
+        else if (rank == 0) mbar_arrive_expect_tx(&b_full[pid], 2u * (uint32_t)p.kch * RO_W2_BOX);
       }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        dead = true;
+        break;
+      }
+      // this CTA's half: vocab rows [n0 + 64 * rank, +64) of W2t
+      if (lane < p.kch)
+        tma_load_2d_pair(sB + (size_t)pid * RO_W2_SLOT + lane * RO_W2_BOX, &mapW2, lane * 64,
+                         n0 + (int)rank * RO_HALF, leader_bar(&b_full[pid]));
     }
     if (dead && lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+    if (pid == 0 && lane == 0) XP_TRACE_MARK(7);
   } else if (warp == RO_WARP_BASE) {
     // ---------------- TMA producer: base tiles (two lanes, one box each) ----------------
     // The latent tile (A) goes first, through the still-empty base ring:
@@ -256,45 +253,40 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
                       m_tile * RO_BM, &base_full[bb]);
       }
     }
+    if (lane == 0) XP_TRACE_MARK(8);
   } else if (warp == 1) {
     // ---------------- MMA issuer (the pair's leader) ----------------
     if (lane == 0 && rank == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(2 * RO_BM, RO_BN, 0, 0);
       bool dead = !mbar_wait_cluster(a_ready, 0);
       tc_fence_after();
-      uint32_t it = 0;
+      const int ksteps = (p.R + 15) / 16;
       for (int t = 0; t < ntiles && !dead; ++t) {
         const uint32_t a = t & 1, u = t >> 1;
-        if (u >= 1 && !mbar_wait_cluster(&acc_empty[a], (u - 1) & 1)) {
+        if ((u >= 1 && !mbar_wait_cluster(&acc_empty[a], (u - 1) & 1)) || !mbar_wait(&b_full[a], u & 1)) {
           dead = true;
           break;
         }
         tc_fence_after();
+        if (t == 0) XP_TRACE_MARK(3);
+        if (t < 16) XP_TRACE_MARK(26 + t);
         const uint32_t d = tmem + RO_TMEM_ACC + a * RO_BN;
-        for (int ks = 0; ks < p.nks && !dead; ++ks, ++it) {
-          const uint32_t s = it % RO_STAGES, k = it / RO_STAGES;
-          if (!mbar_wait(&b_full[s], k & 1)) {
-            dead = true;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t b_base = smem_u32(sB + (size_t)s * RO_B_STAGE);
-          int ksteps = (p.R - ks * RO_KS + 15) / 16;
-          if (ksteps > RO_KS / 16) ksteps = RO_KS / 16;
-          for (int kk = 0; kk < ksteps; ++kk) {
-            // A: TMEM columns hold K pairs; a K step of 16 is 8 columns.
-            const uint32_t a_tm = tmem + RO_TMEM_A + ks * (RO_KS / 2) + kk * 8;
-            // B: K-major (W2t rows), 128-byte rows, 8-row groups 1024 B apart;
-            // a K step of 16 advances 32 bytes inside a 64-wide box.
-            const uint64_t bdesc = smem_desc_sw128(b_base + (kk >> 2) * RO_W2_BOX + (kk & 3) * 32, 16, 1024);
-            tc_mma_f16_ts_pair(d, a_tm, bdesc, idesc, (ks | kk) != 0);
-          }
-          tc_commit_pair(&b_empty[s], 0x3);
+        // A: TMEM columns hold K pairs; a K step of 16 is 8 columns.
+        // B: K-major (W2t rows), 128-byte rows, 8-row groups 1024 B apart;
+        // a K step of 16 advances 32 bytes inside a 64-wide box.  The
+        // descriptor's address field is in 16-byte units, so the steps are
+        // added to the slot's descriptor directly.
+        const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + (size_t)a * RO_W2_SLOT), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < RO_MAX_KCH * 4; ++kk) {
+          if (kk < ksteps)
+            tc_mma_f16_ts_pair(d, tmem + RO_TMEM_A + kk * 8,
+                               bdesc + (uint64_t)(((kk >> 2) * RO_W2_BOX + (kk & 3) * 32) >> 4), idesc, kk != 0);
         }
-        if (dead) break;
         tc_commit_pair(&acc_full[a], 0x3);
       }
       if (dead) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+      XP_TRACE_MARK(4);
       tc_commit_pair(drain, 0x1);
       (void)mbar_wait(drain, 0);
     }
@@ -346,6 +338,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       tc_fence_before();
       __syncwarp();
       if (lane == 0) arrive_leader(a_ready);
+      if (threadIdx.x == 64) XP_TRACE_MARK(2);
     }
 
     float best = -INFINITY;
@@ -355,10 +348,15 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       const uint32_t a = t & 1, u = t >> 1;
       const uint32_t bb = t % RO_NBASE, kb = t / RO_NBASE;
       const int n0 = (n_begin + t) * RO_BN + h * 64;
-      if (!dead && (!mbar_wait(&base_full[bb], kb & 1) || !mbar_wait(&acc_full[a], u & 1))) {
+      if (!dead && !mbar_wait(&base_full[bb], kb & 1)) {
         dead = true;
         flag_error(p.hdr, XP_DEVERR_TIMEOUT);
       }
+      if (!dead && !mbar_wait(&acc_full[a], u & 1)) {
+        dead = true;
+        flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+      }
+      if (threadIdx.x == 64 && t < 16) XP_TRACE_MARK(42 + t);
       tc_fence_after();
       if (!dead) {
         const bool all_valid = n0 + 64 <= p.V;
@@ -388,6 +386,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
         arrive_leader(&acc_empty[a]);
         mbar_arrive(&base_empty[bb]);
       }
+      if (threadIdx.x == 64 && t < 16) XP_TRACE_MARK(10 + t);
     }
     if (row_ok && bidx >= 0 && !dead) atomicMax(&p.keys[row], make_key(best, (uint32_t)bidx));
     __threadfence();
@@ -399,6 +398,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   // the leader's MMAs are complete (drain) and no remote arrive is in flight
   // once both CTAs are here
   cluster_sync();
+  if (threadIdx.x == 0) XP_TRACE_MARK(5);
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -426,11 +426,12 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
     __syncthreads();
     if (threadIdx.x == 0) p.hdr->done = 0u;
   }
+  if (threadIdx.x == 0) XP_TRACE_MARK(6);
 }
 
 size_t readout_smem_bytes() {
-  return 1024 + (size_t)RO_STAGES * RO_B_STAGE + (size_t)RO_NBASE * RO_BASE_TILE +
-         8 * (2 * RO_STAGES + 2 * RO_NBASE + 9) + 16;
+  return 1024 + (size_t)RO_SLOTS * RO_W2_SLOT + (size_t)RO_NBASE * RO_BASE_TILE +
+         8 * (RO_SLOTS + 2 * RO_NBASE + 9) + 16;
 }
 
 namespace {
@@ -461,8 +462,8 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
                                 int64_t rows, int64_t V, int64_t R, int64_t* blk, int64_t B, int32_t* changed,
                                 void* ws, cudaStream_t stream) {
   if (rows <= 0) return XP_OK;
-  const int nks = (int)((R + RO_KS - 1) / RO_KS);
-  if (4 * nks > RO_MAX_KCH) return XP_ERR_SHAPE;
+  const int kch = (int)((R + 63) / 64);
+  if (kch > RO_MAX_KCH) return XP_ERR_SHAPE;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return XP_ERR_LAUNCH;
   RoDevInfo& info = g_ro_dev[dev];
@@ -492,8 +493,7 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
   p.rows = (int32_t)rows;
   p.V = (int32_t)V;
   p.R = (int32_t)R;
-  p.nks = nks;
-  p.kch = 4 * nks;  // A staged in TMEM up to the last W2 stage, zero beyond R
+  p.kch = kch;  // A staged in TMEM up to the last K chunk, zero beyond R
   p.mp = sp.mp;
   p.nt = sp.nt;
   p.per = sp.per;
@@ -520,3 +520,5 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
 }
 
 }  // namespace xp
+
+XP_TRACE_READER(xp_trace_read_readout)
