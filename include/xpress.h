@@ -136,8 +136,9 @@ XP_API xp_status xp_add_argmax_noalloc(const xp_bf16* d_base, int64_t ld_base, c
  *   lat_out[n,b-1,:] = bf16(u[n,b,:] + m @ Wd)           (b = 1..B-1)
  *
  * d_blk [N,B] int64, d_am1 [N] int64, d_hcache [N,B,R] bf16, d_E [V,D] bf16,
- * d_W_lat [D,R] bf16, d_L [B,B,R] float32 (entries above the diagonal are
- * ignored), d_Wg/d_Wu [R,H] bf16, d_Wd [H,R] bf16, d_lat_out [N,B-1,R] bf16.
+ * d_W_lat [D,R] bf16, d_L [B,B,R] float32 (16-byte aligned like the bf16
+ * pointers; entries above the diagonal are ignored), d_Wg/d_Wu [R,H] bf16,
+ * d_Wd [H,R] bf16, d_lat_out [N,B-1,R] bf16.
  * All dense (no padding).  Constraints (else XP_ERR_SHAPE / XP_ERR_ALIGN):
  * 2 <= B <= 16; 16 <= R <= 512 with R a multiple of 16; D a multiple of 8 in
  * [8, 2^20]; H a multiple of 64 in [64, 2^16]; N*B <= 2^22; V <= 2^30.

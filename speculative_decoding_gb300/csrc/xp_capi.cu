@@ -120,7 +120,7 @@ xp_status check_latent_args(const int64_t* blk, const int64_t* am1, const xp_bf1
   if (!blk || !am1 || !hcache || !E || !W_lat || !L || !Wg || !Wu || !Wd) return XP_ERR_NULL;
   if ((D & 7) || (R & 15) || (H & 63)) return XP_ERR_ALIGN;
   if (!aligned16(hcache) || !aligned16(E) || !aligned16(W_lat) || !aligned16(Wg) || !aligned16(Wu) ||
-      !aligned16(Wd) || ((uintptr_t)L & 3) || ((uintptr_t)blk & 7) || ((uintptr_t)am1 & 7))
+      !aligned16(Wd) || !aligned16(L) || ((uintptr_t)blk & 7) || ((uintptr_t)am1 & 7))
     return XP_ERR_ALIGN;
   return XP_OK;
 }

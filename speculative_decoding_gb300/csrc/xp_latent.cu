@@ -54,29 +54,32 @@ __device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float((uint
 // Shared memory: [0, region) is the stage ring; once the MMAs are done it holds
 // red[128][tn + 4] (this CTA's fp32 partial sums, read by the whole cluster)
 // and xs[128][w] (the reduced x of this CTA's w columns).  After it: Ls (the
-// mixer weights of those columns, lower triangle packed by rows), the token
-// table and the barriers.
+// mixer weights of those columns, lower triangle packed by rows), hcs (the
+// hidden cache of those columns for the tile's 128 rows), the token table and
+// the barriers.  Ls and hcs are copied by the bulk-copy engine at the start,
+// while the reduction runs, so the epilogue reads neither from global memory.
 struct ProjParams {
   const int64_t* blk;
   const int64_t* am1;
-  const uint16_t* hcache;
   const uint16_t* E;
   const float* L;
   float* u;
   uint16_t* ub;
   WsHeader* hdr;
   int32_t N, B, V, D, R, bpt, tn, S, w, chunks, ntiles, stages;
-  uint32_t region;
+  uint32_t region, hc_off, tok_off, bar_off;
 };
 
 __host__ __device__ inline uint32_t proj_ls_bytes(int B, int w) {
-  return (uint32_t)(((B * (B + 1) / 2) * w * 4 + 15) & ~15);
+  return (uint32_t)(((B * (B + 1) / 2) * w * 4 + 127) & ~127);
 }
 
 __global__ void __launch_bounds__(LT_THREADS, 2)
-proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p) {
+proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_constant__ CUtensorMap mapHc,
+                const ProjParams p) {
   extern __shared__ uint8_t smem_raw[];
   if (threadIdx.x == 0) XP_TRACE_MARK(0);
+  if (threadIdx.x == 0) XP_TRACE_SM(15);
   uint8_t* smem = align1024(smem_raw);
   const uint32_t b_bytes = (uint32_t)p.tn * LT_BK * 2;
   const uint32_t stage_bytes = LT_A_CHUNK + b_bytes;
@@ -84,11 +87,13 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
   float* red = reinterpret_cast<float*>(smem);
   float* xs = red + LT_BM * ld;
   float* Ls = reinterpret_cast<float*>(smem + p.region);
-  int64_t* tok = reinterpret_cast<int64_t*>(smem + p.region + proj_ls_bytes(p.B, p.w));
-  uint64_t* full = reinterpret_cast<uint64_t*>(tok + LT_BM);
+  const uint16_t* hcs = reinterpret_cast<const uint16_t*>(smem + p.hc_off);
+  int64_t* tok = reinterpret_cast<int64_t*>(smem + p.tok_off);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
   uint64_t* empty = full + p.stages;
   uint64_t* acc_full = empty + p.stages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  uint64_t* aux_full = acc_full + 1;  // Ls and hcs landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_full + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ks = (int)(blockIdx.x % p.S);
@@ -99,13 +104,17 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
   const int c_lo = ks * p.w;                   // this CTA's columns of the tile: [c_lo, c_lo + w)
   const int col0 = nt * p.tn + c_lo;           // ... as latent channels
   const int nbl = min(p.bpt, p.N - mt * p.bpt);  // blocks of this M tile
+  // channels of this CTA's slice that exist (R is a multiple of 16, the
+  // slice starts at a multiple of 8): 0 or a multiple of 8
+  const int wv = max(0, min(p.w, p.R - col0));
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
-      mbar_init(&full[s], 2);  // the gathering warp + the W_lat TMA
+      mbar_init(&full[s], 4 + 1);  // the four gathering warps + the W_lat TMA
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
+    mbar_init(aux_full, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -118,20 +127,47 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) XP_TRACE_MARK(1);
   pdl_launch_dependents();
-  pdl_wait();  // blk may have been written by the preceding pass
-  if (threadIdx.x == 0) XP_TRACE_MARK(2);
 
   if (warp == 0) {
-    // lane 0 waits for the stage and arms its barrier; lanes 0..tn/64-1 then
-    // issue one W_lat box each (a single thread issues tiled copies slowly)
-    if (lane == 0) prefetch_tensormap(&mapWlat);
+    // Nothing this warp reads is written by the preceding kernels, so it
+    // starts before the dependency wait: the mixer weights (one bulk copy
+    // per (b, j) pair of the lower triangle: the slice's wv channels), the
+    // hidden-cache slice (one tensor box), then the W_lat ring.  Lane 0
+    // waits for a stage and arms its barrier; lanes 0..tn/64-1 issue one
+    // W_lat box each (a single thread issues tiled copies slowly).
+    const int tri = p.B * (p.B + 1) / 2;
+    // the copy engine serves requests in order: the first W_lat stages go
+    // first, the epilogue's operands (needed only after the MMAs) after them
+    auto aux_copies = [&]() {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(aux_full, (uint32_t)(tri * wv * 4) + (uint32_t)(LT_BM * p.w * 2));
+        tma_load_2d(smem + p.hc_off, &mapHc, col0, mt * p.bpt * p.B, aux_full);
+      }
+      __syncwarp();
+      if (wv > 0) {
+        for (int pr = lane; pr < tri; pr += 32) {
+          int b = 0;
+          while ((b + 1) * (b + 2) / 2 <= pr) ++b;
+          const int j = pr - b * (b + 1) / 2;
+          bulk_load(Ls + pr * p.w, p.L + ((int64_t)b * p.B + j) * p.R + col0, (uint32_t)wv * 4, aux_full);
+        }
+      }
+    };
+    const uint64_t pol = policy_evict_last();  // every pass re-reads W_lat
+    if (lane == 0) {
+      prefetch_tensormap(&mapWlat);
+      prefetch_tensormap(&mapHc);
+    }
+    // the W_lat boxes beyond the ring's first round: into L2 now
+    for (int i = p.stages + lane / (p.tn / 64); i < nck; i += 32 / (p.tn / 64))
+      tma_prefetch_2d(&mapWlat, nt * p.tn + (lane % (p.tn / 64)) * 64, (c0 + i) * LT_BK);
     for (int i = 0; i < nck; ++i) {
+      if (i == p.stages) aux_copies();
       const uint32_t s = i % p.stages, k = i / p.stages;
       int ok = 1;
       if (lane == 0) {
         if (k >= 1 && !mbar_wait(&empty[s], (k - 1) & 1)) ok = 0;
         else mbar_arrive_expect_tx(&full[s], b_bytes);
-        if (k >= 1 && i - p.stages < 8) XP_TRACE_MARK(48 + i - p.stages);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
@@ -139,9 +175,10 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
         break;
       }
       if (lane < p.tn / 64)
-        tma_load_2d(smem + (size_t)s * stage_bytes + LT_A_CHUNK + lane * LT_BOX, &mapWlat, nt * p.tn + lane * 64,
-                    (c0 + i) * LT_BK, &full[s]);
+        tma_load_2d_hint(smem + (size_t)s * stage_bytes + LT_A_CHUNK + lane * LT_BOX, &mapWlat,
+                         nt * p.tn + lane * 64, (c0 + i) * LT_BK, &full[s], pol);
     }
+    if (nck <= p.stages) aux_copies();
     if (lane == 0) XP_TRACE_MARK(3);
   } else if (warp == 1) {
     if (lane == 0) {
@@ -155,7 +192,6 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
         }
         tc_fence_after();
         if (i == 0) XP_TRACE_MARK(7);
-        if (i < 7) XP_TRACE_MARK(56 + i);
         const uint32_t a_base = smem_u32(smem + (size_t)s * stage_bytes);
         const uint32_t b_base = a_base + LT_A_CHUNK;
 #pragma unroll
@@ -169,12 +205,11 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
       if (dead) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
       tc_commit(acc_full);
       XP_TRACE_MARK(8);
-#ifdef XP_TRACE
-      if (mbar_wait(acc_full, 0)) XP_TRACE_MARK(15);
-#endif
     }
   } else {
     const int et = threadIdx.x - 64;  // 0..127
+    pdl_wait();  // blk may have been written by the preceding pass
+    if (et == 0) XP_TRACE_MARK(2);
     // token of every row of the tile (-1: no block there)
     {
       const int bl = et / p.B, b = et - bl * p.B, n = mt * p.bpt + bl;
@@ -189,47 +224,51 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
       tok[et] = t;
     }
     named_barrier_sync(1, 128);
-    if (threadIdx.x == 64) XP_TRACE_MARK(4);
-    // gather: warp gw owns the stages s with s % 4 == gw and refills them in
-    // order.  Eight lanes cover one 128-byte row piece, so each copy
-    // instruction reads four whole rows; cp.async keeps all 32 copies of a
-    // lane in flight without registers.
+    if (et == 0) XP_TRACE_MARK(4);
+    // gather: every warp fills its 32 rows of every stage.  Eight lanes cover
+    // one 128-byte row piece, so each copy instruction reads four whole
+    // rows; a stage's copies form one cp.async group, and a warp hands a
+    // stage over (wait for its group, proxy fence, arrive) only when it is
+    // LAG stages ahead, so up to LAG + 1 stages per warp are in flight.
     const int gw = warp - 2, rsub = lane >> 3, piece = lane & 7;
+    bool dead = false;
+    auto hand_over = [&](int i) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[i % p.stages]);
+      if (lane == 0 && i == 0) XP_TRACE_MARK(5);
+      if (lane == 0 && i == nck - 1) XP_TRACE_MARK(6);
+    };
+    const int lag = p.stages - 1;  // 1 or 2 (stages is 2 or 3)
     for (int i = 0; i < nck; ++i) {
-      const int s = i % p.stages;
-      if (s % 4 != gw) continue;
-      const int k = i / p.stages;
+      const int s = i % p.stages, k = i / p.stages;
       if (k >= 1 && !mbar_wait(&empty[s], (k - 1) & 1)) {
-        flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+        dead = true;
         break;
       }
       uint8_t* dst = smem + (size_t)s * stage_bytes;
       const int kel = (c0 + i) * LT_BK + piece * 8;
       const bool kin = kel < p.D;  // D is a multiple of 8: a piece is wholly in or out
-#pragma unroll 8
-      for (int it = 0; it < LT_BM / 4; ++it) {
-        const int r = it * 4 + rsub;
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int r = gw * 32 + it * 4 + rsub;
         const int64_t t = tok[r];
         const bool ok = kin && t >= 0;
         cp_async_16(dst + r * 128 + ((piece ^ (r & 7)) << 4), ok ? p.E + t * p.D + kel : p.E, ok ? 16u : 0u);
       }
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&full[s]);
-      if (lane == 0 && i == 0) XP_TRACE_MARK(5);
-      if (lane == 0 && i == nck - 1) XP_TRACE_MARK(6);
+      cp_async_commit();
+      if (i >= lag) {
+        if (lag == 2) cp_async_wait_group<2>();
+        else cp_async_wait_group<1>();
+        hand_over(i - lag);
+      }
     }
-    // the mixer weights of this CTA's columns, copied in the background while
-    // the MMAs finish (waited for before the mixer)
-    const int tri = p.B * (p.B + 1) / 2;
-    for (int e = et; e < tri * p.w; e += 128) {
-      const int pr = e / p.w, c = e - pr * p.w;
-      int b = 0;
-      while ((b + 1) * (b + 2) / 2 <= pr) ++b;
-      const int j = pr - b * (b + 1) / 2;
-      const bool in = col0 + c < p.R;
-      cp_async_4(Ls + e, in ? p.L + ((int64_t)b * p.B + j) * p.R + col0 + c : p.L, in ? 4u : 0u);
+    if (dead) {
+      flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+      cp_async_wait_all();
+    } else {
+      cp_async_wait_all();
+      for (int i = max(0, nck - lag); i < nck; ++i) hand_over(i);
     }
   }
 
@@ -257,13 +296,13 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
   if (warp >= 2) {
     const int et = threadIdx.x - 64;
     if (et == 0) XP_TRACE_MARK(11);
+    if (!mbar_wait(aux_full, 0)) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
     // ---- epilogue 2: x = hcache + sum of the cluster's partials (fixed
     // order) for this CTA's columns of all rows; two (row, 4 columns) items
     // per thread per round, every partial requested before any is used
     const int wq = p.w / 4, items = LT_BM * wq;
     for (int i0 = et; i0 < items; i0 += 256) {
       float4 v[2][LT_MAX_S];
-      uint2 hc[2];
       int rr[2], gg[2];
       bool on[2];
 #pragma unroll
@@ -271,12 +310,8 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
         const int it = i0 + h * 128;
         rr[h] = it / wq;
         gg[h] = it - rr[h] * wq;
-        const int bl = rr[h] / p.B, b = rr[h] - bl * p.B;
+        const int bl = rr[h] / p.B;
         on[h] = it < items && bl < nbl;
-        const int col = col0 + 4 * gg[h];
-        hc[h] = make_uint2(0u, 0u);
-        if (on[h] && col < p.R)
-          hc[h] = *reinterpret_cast<const uint2*>(p.hcache + ((int64_t)(mt * p.bpt + bl) * p.B + b) * p.R + col);
 #pragma unroll
         for (int q = 0; q < LT_MAX_S; ++q)
           v[h][q] = (on[h] && q < p.S) ? ld_dsmem_v4(red + rr[h] * ld + c_lo + 4 * gg[h], (uint32_t)q)
@@ -295,22 +330,23 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
             a.w += v[h][q].w;
           }
         }
+        // the hidden cache of these 4 channels (zero past R: TMA fill)
+        const uint2 hc = *reinterpret_cast<const uint2*>(hcs + rr[h] * p.w + 4 * gg[h]);
         float4 x;
-        x.x = bf16lo_to_f32(hc[h].x) + a.x;
-        x.y = bf16hi_to_f32(hc[h].x) + a.y;
-        x.z = bf16lo_to_f32(hc[h].y) + a.z;
-        x.w = bf16hi_to_f32(hc[h].y) + a.w;
+        x.x = bf16lo_to_f32(hc.x) + a.x;
+        x.y = bf16hi_to_f32(hc.x) + a.y;
+        x.z = bf16lo_to_f32(hc.y) + a.z;
+        x.w = bf16hi_to_f32(hc.y) + a.w;
         *reinterpret_cast<float4*>(xs + rr[h] * p.w + 4 * gg[h]) = x;
       }
     }
-    if (et == 0) XP_TRACE_MARK(12);
-    cp_async_wait_all();  // this thread's share of Ls
+    if (et == 127) XP_TRACE_MARK(12);
     named_barrier_sync(1, 128);
     // ---- the causal mixer on this CTA's columns: u[b] = sum_{j<=b} L[b,j] x[j]
     for (int it = et; it < nbl * p.w; it += 128) {
       const int bl = it / p.w, c = it - bl * p.w;
       const int col = col0 + c;
-      if (col >= p.R) continue;
+      if (c >= wv) continue;
       const int n = mt * p.bpt + bl;
       float x[LT_MAX_B];
 #pragma unroll
@@ -330,7 +366,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const ProjParams p)
     }
     if (et == 0) XP_TRACE_MARK(13);
   }
-  cluster_sync();  // the peers have finished reading this CTA's partial sums
+  cluster_sync_relaxed();  // the peers have finished reading this CTA's partial sums
   if (threadIdx.x == 0) XP_TRACE_MARK(14);
   if (warp == 1) {
     tc_fence_after();
@@ -381,17 +417,30 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) XP_TRACE_MARK(17);
   pdl_launch_dependents();
-  pdl_wait();  // ub comes from proj_mix
-  if (threadIdx.x == 0) XP_TRACE_MARK(18);
 
   if (warp == 0) {
-    // lane 0 arms the stage; lanes 0, 1, 2 issue the ub, Wg and Wu boxes
+    // lane 0 arms the stage; lanes 0, 1, 2 issue the ub, Wg and Wu boxes.
+    // The weights of the first stages are requested before the dependency
+    // wait (nothing earlier in the pass writes them); ub comes from proj_mix.
     if (lane == 0) {
       prefetch_tensormap(&mapUb);
       prefetch_tensormap(&mapWg);
       prefetch_tensormap(&mapWu);
     }
-    for (int i = 0; i < p.chunks; ++i) {
+    const uint64_t pol = policy_evict_last();  // every pass re-reads Wg, Wu
+    const int pre = p.chunks < p.stages ? p.chunks : p.stages;
+    for (int i = 0; i < pre; ++i) {
+      uint8_t* dst = smem + (size_t)i * stage_bytes;
+      if (lane == 0) mbar_arrive_expect_tx(&full[i], stage_bytes);
+      __syncwarp();
+      if (lane == 1) tma_load_2d_hint(dst + LT_A_CHUNK, &mapWg, ht * 64, i * LT_BK, &full[i], pol);
+      if (lane == 2) tma_load_2d_hint(dst + LT_A_CHUNK + LT_BOX, &mapWu, ht * 64, i * LT_BK, &full[i], pol);
+    }
+    pdl_wait();
+    if (lane == 0) XP_TRACE_MARK(18);
+    if (lane == 0)
+      for (int i = 0; i < pre; ++i) tma_load_2d(smem + (size_t)i * stage_bytes, &mapUb, i * LT_BK, mt * LT_BM, &full[i]);
+    for (int i = pre; i < p.chunks; ++i) {
       const uint32_t s = i % p.stages, k = i / p.stages;
       int ok = 1;
       if (lane == 0) {
@@ -405,8 +454,8 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
       }
       uint8_t* dst = smem + (size_t)s * stage_bytes;
       if (lane == 0) tma_load_2d(dst, &mapUb, i * LT_BK, mt * LT_BM, &full[s]);
-      if (lane == 1) tma_load_2d(dst + LT_A_CHUNK, &mapWg, ht * 64, i * LT_BK, &full[s]);
-      if (lane == 2) tma_load_2d(dst + LT_A_CHUNK + LT_BOX, &mapWu, ht * 64, i * LT_BK, &full[s]);
+      if (lane == 1) tma_load_2d_hint(dst + LT_A_CHUNK, &mapWg, ht * 64, i * LT_BK, &full[s], pol);
+      if (lane == 2) tma_load_2d_hint(dst + LT_A_CHUNK + LT_BOX, &mapWu, ht * 64, i * LT_BK, &full[s], pol);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -436,6 +485,7 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
       XP_TRACE_MARK(20);
     }
   } else {
+    pdl_wait();
     if (!mbar_wait(acc_full, 0)) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
     tc_fence_after();
     if (threadIdx.x == 64) XP_TRACE_MARK(21);
@@ -476,27 +526,32 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
 // ============================================================================
 // Shared memory: [0, region) is the stage ring, then red[128][tn + 4] (this
 // CTA's fp32 partial sums, read by the whole cluster); barriers after it.
+// Shared memory: [0, region) is the stage ring, then red[128][tn + 4] (this
+// CTA's fp32 partial sums, read by the whole cluster) reusing it; us (the
+// residual u of this CTA's w columns for the tile's 128 rows, copied by TMA
+// while the MMAs run); the barriers.
 struct DownParams {
-  const float* u;
   uint16_t* lat;
   WsHeader* hdr;
   int32_t N, B, R, tn, S, w, chunks, ntiles, stages;
-  uint32_t region;
+  uint32_t region, bar_off;
 };
 
 __global__ void __launch_bounds__(LT_THREADS, 2)
 mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant__ CUtensorMap mapWd,
-                const DownParams p) {
+                const __grid_constant__ CUtensorMap mapU, const DownParams p) {
   extern __shared__ uint8_t smem_raw[];
   if (threadIdx.x == 0) XP_TRACE_MARK(32);
   uint8_t* smem = align1024(smem_raw);
   const uint32_t b_bytes = (uint32_t)p.tn * LT_BK * 2;
   const uint32_t stage_bytes = LT_A_CHUNK + b_bytes;
   const int ld = p.tn + 4;  // floats per row of red (a 16-byte multiple)
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.region);
+  const float* us = reinterpret_cast<const float*>(smem + p.region);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
   uint64_t* empty = full + p.stages;
   uint64_t* acc_full = empty + p.stages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  uint64_t* aux_full = acc_full + 1;  // us landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_full + 1);
   float* red = reinterpret_cast<float*>(smem);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -515,6 +570,7 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
+    mbar_init(aux_full, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -527,16 +583,35 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) XP_TRACE_MARK(33);
   pdl_launch_dependents();
-  pdl_wait();  // m comes from mlp_up
-  if (threadIdx.x == 0) XP_TRACE_MARK(34);
 
   if (warp == 0) {
-    // lane 0 arms the stage; lane 0 issues the m box, lanes 1.. the Wd boxes
+    // lane 0 arms the stage; lane 0 issues the m box, lanes 1.. the Wd boxes.
+    // The Wd boxes of the first stages are requested before the dependency
+    // wait (nothing earlier in the pass writes Wd); m comes from mlp_up and
+    // the residual u (one box of this CTA's columns) from proj_mix.
     if (lane == 0) {
       prefetch_tensormap(&mapM);
       prefetch_tensormap(&mapWd);
+      prefetch_tensormap(&mapU);
     }
-    for (int i = 0; i < nck; ++i) {
+    const uint64_t pol = policy_evict_last();  // every pass re-reads Wd
+    const int pre = nck < p.stages ? nck : p.stages;
+    for (int i = 0; i < pre; ++i) {
+      uint8_t* dst = smem + (size_t)i * stage_bytes;
+      if (lane == 0) mbar_arrive_expect_tx(&full[i], stage_bytes);
+      __syncwarp();
+      if (lane >= 1 && lane <= p.tn / 64)
+        tma_load_2d_hint(dst + LT_A_CHUNK + (lane - 1) * LT_BOX, &mapWd, nt * p.tn + (lane - 1) * 64, (c0 + i) * LT_BK,
+                         &full[i], pol);
+    }
+    pdl_wait();
+    if (lane == 0) {
+      XP_TRACE_MARK(34);
+      for (int i = 0; i < pre; ++i) tma_load_2d(smem + (size_t)i * stage_bytes, &mapM, (c0 + i) * LT_BK, mt * LT_BM, &full[i]);
+      mbar_arrive_expect_tx(aux_full, (uint32_t)(LT_BM * p.w * 4));
+      tma_load_2d(smem + p.region, &mapU, col0, mt * LT_BM, aux_full);
+    }
+    for (int i = pre; i < nck; ++i) {
       const uint32_t s = i % p.stages, k = i / p.stages;
       int ok = 1;
       if (lane == 0) {
@@ -551,8 +626,8 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
       uint8_t* dst = smem + (size_t)s * stage_bytes;
       if (lane == 0) tma_load_2d(dst, &mapM, (c0 + i) * LT_BK, mt * LT_BM, &full[s]);
       if (lane >= 1 && lane <= p.tn / 64)
-        tma_load_2d(dst + LT_A_CHUNK + (lane - 1) * LT_BOX, &mapWd, nt * p.tn + (lane - 1) * 64, (c0 + i) * LT_BK,
-                    &full[s]);
+        tma_load_2d_hint(dst + LT_A_CHUNK + (lane - 1) * LT_BOX, &mapWd, nt * p.tn + (lane - 1) * 64, (c0 + i) * LT_BK,
+                         &full[s], pol);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -581,6 +656,7 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
       XP_TRACE_MARK(32 + 8);
     }
   } else {
+    pdl_wait();
     if (!mbar_wait(acc_full, 0)) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
     tc_fence_after();
     if (threadIdx.x == 64) XP_TRACE_MARK(41);
@@ -607,6 +683,7 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
   if (warp >= 2) {
     const int et = threadIdx.x - 64;
     const int wq = p.w / 4, items = LT_BM * wq;
+    if (!mbar_wait(aux_full, 0)) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
     for (int i0 = et; i0 < items; i0 += 256) {
       float4 v[2][LT_MAX_S], uu[2];
       int64_t dst[2];
@@ -620,8 +697,7 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
         const int col = col0 + 4 * gg;
         on[h] = it < items && grow < rows && b >= 1 && col < p.R;
         dst[h] = ((int64_t)n * (p.B - 1) + b - 1) * p.R + col;
-        uu[h] = on[h] ? *reinterpret_cast<const float4*>(p.u + (int64_t)grow * p.R + col)
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        uu[h] = on[h] ? *reinterpret_cast<const float4*>(us + rr * p.w + 4 * gg) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int q = 0; q < LT_MAX_S; ++q)
           v[h][q] = (on[h] && q < p.S) ? ld_dsmem_v4(red + rr * ld + c_lo + 4 * gg, (uint32_t)q)
@@ -644,9 +720,9 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
             make_uint2(f32x2_to_bf16x2(uu[h].x + a.x, uu[h].y + a.y), f32x2_to_bf16x2(uu[h].z + a.z, uu[h].w + a.w));
       }
     }
-    if (et == 0) XP_TRACE_MARK(44);
+    if (et == 127) XP_TRACE_MARK(44);
   }
-  cluster_sync();
+  cluster_sync_relaxed();  // the peers have finished reading this CTA's partial sums
   if (threadIdx.x == 0) XP_TRACE_MARK(45);
   if (warp == 1) {
     tc_fence_after();
@@ -749,7 +825,6 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     ProjParams p;
     p.blk = blk;
     p.am1 = am1;
-    p.hcache = hcache;
     p.E = E;
     p.L = L;
     p.u = u;
@@ -768,20 +843,30 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     p.ntiles = ntiles;
     const uint32_t stage_bytes = LT_A_CHUNK + (uint32_t)tn * LT_BK * 2;
     const size_t red_xs = (size_t)LT_BM * (tn + 4) * 4 + (size_t)LT_BM * p.w * 4;
-    const size_t tail = proj_ls_bytes((int)B, p.w) + 8 * LT_BM;  // Ls + token table
+    const size_t ls = proj_ls_bytes((int)B, p.w);
+    const size_t hc = ((size_t)LT_BM * p.w * 2 + 127) & ~size_t(127);
     auto region_of = [&](int st) {
       const size_t ring = (size_t)st * stage_bytes;
       return (ring > red_xs ? ring : red_xs + 1023) & ~size_t(1023);
     };
-    auto total = [&](int st) { return 1024 + region_of(st) + tail + 8 * (2 * st + 1) + 16; };
+    // Ls, hcs, the token table, then full/empty per stage, acc_full,
+    // aux_full and the TMEM address slot
+    auto total = [&](int st) { return 1024 + region_of(st) + ls + hc + 8 * LT_BM + 8 * (2 * st + 2) + 16; };
+    // the gathering warps keep stages - 1 stages in flight: 2 or 3 stages
     const int per_cta = (p.chunks + p.S - 1) / p.S;
-    p.stages = pick_stages(stage_bytes, per_cta, total);
+    p.stages = per_cta >= 3 ? 3 : 2;
+    if (p.stages == 3 && total(3) > kTwoPerSm) p.stages = 2;
     p.region = (uint32_t)region_of(p.stages);
+    p.hc_off = p.region + (uint32_t)ls;
+    p.tok_off = p.hc_off + (uint32_t)hc;
+    p.bar_off = p.tok_off + 8 * LT_BM;
     const size_t smem = total(p.stages);
     const int mtiles = (int)((N + p.bpt - 1) / p.bpt);
-    CUtensorMap mapWlat;
-    if (!cached_map_bf16_2d(&mapWlat, W_lat, (uint64_t)R, (uint64_t)D, (uint64_t)R, 64, LT_BK)) return XP_ERR_LAUNCH;
-    void* args[] = {&mapWlat, &p};
+    CUtensorMap mapWlat, mapHc;
+    if (!cached_map_bf16_2d(&mapWlat, W_lat, (uint64_t)R, (uint64_t)D, (uint64_t)R, 64, LT_BK) ||
+        !cached_map_plain_2d(&mapHc, hcache, 2, (uint64_t)R, (uint64_t)(N * B), (uint64_t)R, (uint32_t)p.w, LT_BM))
+      return XP_ERR_LAUNCH;
+    void* args[] = {&mapWlat, &mapHc, &p};
     if (launch_ex((const void*)proj_mix_kernel, dim3((unsigned)(mtiles * ntiles * p.S)), smem, stream, p.S, args) !=
         cudaSuccess)
       return XP_ERR_LAUNCH;
@@ -811,7 +896,6 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
   // ---- mlp_down
   {
     DownParams p;
-    p.u = u;
     p.lat = lat_out;
     p.hdr = hdr;
     p.N = (int32_t)N;
@@ -828,17 +912,21 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
       const size_t ring = (size_t)st * stage_bytes;
       return (ring > red_bytes ? ring : red_bytes + 1023) & ~size_t(1023);
     };
-    auto total = [&](int st) { return 1024 + region_of(st) + 8 * (2 * st + 1) + 16; };
+    const size_t us_bytes = (size_t)LT_BM * p.w * 4;
+    // us, then full/empty per stage, acc_full, aux_full and the TMEM slot
+    auto total = [&](int st) { return 1024 + region_of(st) + us_bytes + 8 * (2 * st + 2) + 16; };
     const int per_cta = (p.chunks + p.S - 1) / p.S;
     p.stages = pick_stages(stage_bytes, per_cta, total);
     p.region = (uint32_t)region_of(p.stages);
+    p.bar_off = p.region + (uint32_t)us_bytes;
     const size_t smem = total(p.stages);
     const int mtiles = (rows + LT_BM - 1) / LT_BM;
-    CUtensorMap mapM, mapWd;
+    CUtensorMap mapM, mapWd, mapU;
     if (!cached_map_bf16_2d(&mapM, m, (uint64_t)H, (uint64_t)rows, (uint64_t)H, LT_BK, LT_BM) ||
-        !cached_map_bf16_2d(&mapWd, Wd, (uint64_t)R, (uint64_t)H, (uint64_t)R, 64, LT_BK))
+        !cached_map_bf16_2d(&mapWd, Wd, (uint64_t)R, (uint64_t)H, (uint64_t)R, 64, LT_BK) ||
+        !cached_map_plain_2d(&mapU, u, 4, (uint64_t)R, (uint64_t)rows, (uint64_t)R, (uint32_t)p.w, LT_BM))
       return XP_ERR_LAUNCH;
-    void* args[] = {&mapM, &mapWd, &p};
+    void* args[] = {&mapM, &mapWd, &mapU, &p};
     if (launch_ex((const void*)mlp_down_kernel, dim3((unsigned)(mtiles * ntiles * p.S)), smem, stream, p.S, args) !=
         cudaSuccess)
       return XP_ERR_LAUNCH;

@@ -168,6 +168,14 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) XP_TRACE_MARK(1);
+  // Programmatic dependent launch: the next kernel in the stream (the next
+  // pass's first latent kernel) may start its prologue as SMs free up; it
+  // waits for this grid before it reads blk.  This grid, in turn, may have
+  // started while the latent stage was still running: only the W2 producers
+  // and the base producer's L2 prefetch (W2t and base are never written by a
+  // pass) run ahead of the wait below.
+  pdl_launch_dependents();
+  if (warp != 0 && warp != RO_WARP_W2B && warp != RO_WARP_BASE) pdl_wait();
   // the leader's copy of a barrier, as a shared::cluster address
   auto leader_bar = [](uint64_t* b) { return mapa_shared(smem_u32(b), 0u); };
   // arrive on the leader's copy of a barrier (locally in the leader)
@@ -185,6 +193,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
     // each (a single thread issues tiled copies slowly).
     const int pid = warp == 0 ? 0 : 1;
     if (pid == 0 && lane == 0) prefetch_tensormap(&mapW2);
+    const uint64_t pol = policy_evict_first();  // read once per pass
     bool dead = false;
     for (int t = pid; t < ntiles; t += RO_SLOTS) {
       const int n0 = (n_begin + t) * RO_BN;
@@ -201,8 +210,10 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       // this CTA's half: vocab rows [n0 + 64 * rank, +64) of W2t
       if (lane < p.kch)
         tma_load_2d_pair(sB + (size_t)pid * RO_W2_SLOT + lane * RO_W2_BOX, &mapW2, lane * 64,
-                         n0 + (int)rank * RO_HALF, leader_bar(&b_full[pid]));
+                         n0 + (int)rank * RO_HALF, leader_bar(&b_full[pid]), pol);
+      if (t == pid) pdl_wait();  // after the first tile of this slot is requested
     }
+    pdl_wait();  // returns at once if already passed above
     if (dead && lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
     if (pid == 0 && lane == 0) XP_TRACE_MARK(7);
   } else if (warp == RO_WARP_BASE) {
@@ -212,7 +223,15 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
     // the epilogue warps before the ring is reused.
     const int rounds = (p.kch + 3) / 4;
     bool a_dead = false;
-    if (lane == 0) prefetch_tensormap(&mapLat);
+    const uint64_t pol_base = policy_evict_first();  // read once per pass
+    if (lane == 0) {
+      prefetch_tensormap(&mapLat);
+      prefetch_tensormap(&mapBase);
+    }
+    // the first base tiles into L2 while the latent is still being computed
+    if (lane < 2 * RO_NBASE && lane / 2 < ntiles)
+      tma_prefetch_2d(&mapBase, (n_begin + lane / 2) * RO_BN + (lane & 1) * 64, m_tile * RO_BM);
+    pdl_wait();
     for (int r = 0; r < rounds && !a_dead; ++r) {
       const int nbox = p.kch - 4 * r < 4 ? p.kch - 4 * r : 4;
       int ok = 1;
@@ -235,7 +254,6 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
     if (a_dead) {
       if (lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
     } else {
-      if (lane == 0) prefetch_tensormap(&mapBase);
       for (int t = 0; t < ntiles; ++t) {
         const int n0 = (n_begin + t) * RO_BN;
         const uint32_t bb = t % RO_NBASE, k = t / RO_NBASE;
@@ -249,8 +267,8 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
           break;
         }
         if (lane < 2)
-          tma_load_2d(sBase + (size_t)bb * RO_BASE_TILE + lane * RO_BASE_BOX, &mapBase, n0 + lane * 64,
-                      m_tile * RO_BM, &base_full[bb]);
+          tma_load_2d_hint(sBase + (size_t)bb * RO_BASE_TILE + lane * RO_BASE_BOX, &mapBase, n0 + lane * 64,
+                           m_tile * RO_BM, &base_full[bb], pol_base);
       }
     }
     if (lane == 0) XP_TRACE_MARK(8);
@@ -263,12 +281,21 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       const int ksteps = (p.R + 15) / 16;
       for (int t = 0; t < ntiles && !dead; ++t) {
         const uint32_t a = t & 1, u = t >> 1;
-        if ((u >= 1 && !mbar_wait_cluster(&acc_empty[a], (u - 1) & 1)) || !mbar_wait(&b_full[a], u & 1)) {
+        if (u >= 1 && !mbar_wait_cluster(&acc_empty[a], (u - 1) & 1)) {
+          dead = true;
+          break;
+        }
+        if (t < 16) XP_TRACE_MARK(42 + t);
+        if (!mbar_wait(&b_full[a], u & 1)) {
           dead = true;
           break;
         }
         tc_fence_after();
         if (t == 0) XP_TRACE_MARK(3);
+#ifdef XP_TRACE
+        if (t == 0 || t == ntiles - 1) g_trace[blockIdx.x * kTraceSlots + 58 + (t != 0)] = clock64();
+        if (t == ntiles - 1) XP_TRACE_MARK(60);
+#endif
         if (t < 16) XP_TRACE_MARK(26 + t);
         const uint32_t d = tmem + RO_TMEM_ACC + a * RO_BN;
         // A: TMEM columns hold K pairs; a K step of 16 is 8 columns.
@@ -356,7 +383,6 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
         dead = true;
         flag_error(p.hdr, XP_DEVERR_TIMEOUT);
       }
-      if (threadIdx.x == 64 && t < 16) XP_TRACE_MARK(42 + t);
       tc_fence_after();
       if (!dead) {
         const bool all_valid = n0 + 64 <= p.V;
@@ -504,17 +530,19 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
   p.keys = w.keys;
   p.hdr = w.hdr;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = 2;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3((unsigned int)(2 * p.mp * per));
   cfg.blockDim = dim3(RO_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, readout_argmax_kernel, mapW2, mapBase, mapLat, p) != cudaSuccess) return XP_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? XP_OK : XP_ERR_LAUNCH;
 }

@@ -40,6 +40,24 @@ inline bool make_map_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner, 
   return r == CUDA_SUCCESS;
 }
 
+// 2-D tensor [outer, inner] of 2- or 4-byte elements (bf16 or fp32), row
+// pitch `ld` elements, box [box_outer, box_inner] without swizzle (the box
+// lands in shared memory as dense rows of box_inner elements; box_inner *
+// elem_bytes must be a multiple of 16).  Out-of-range elements read as zero.
+inline bool make_map_plain_2d(CUtensorMap* map, const void* ptr, uint32_t elem_bytes, uint64_t inner, uint64_t outer,
+                              uint64_t ld, uint32_t box_inner, uint32_t box_outer) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * elem_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = enc(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // make_map_bf16_2d through a small per-thread cache keyed on every argument,
 // so repeated calls on the same buffers skip the encode.
 inline bool cached_map_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
@@ -61,6 +79,36 @@ inline bool cached_map_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner
   if (!make_map_bf16_2d(map, ptr, inner, outer, ld, box_inner, box_outer)) return false;
   Entry& e = cache[next++ % 16];
   e.ptr = ptr;
+  e.inner = inner;
+  e.outer = outer;
+  e.ld = ld;
+  e.bi = box_inner;
+  e.bo = box_outer;
+  e.map = *map;
+  return true;
+}
+
+// make_map_plain_2d through its own small per-thread cache.
+inline bool cached_map_plain_2d(CUtensorMap* map, const void* ptr, uint32_t elem_bytes, uint64_t inner,
+                                uint64_t outer, uint64_t ld, uint32_t box_inner, uint32_t box_outer) {
+  struct Entry {
+    const void* ptr;
+    uint64_t inner, outer, ld;
+    uint32_t eb, bi, bo;
+    CUtensorMap map;
+  };
+  static thread_local Entry cache[8];
+  static thread_local unsigned next = 0;
+  for (auto& e : cache)
+    if (e.ptr == ptr && e.eb == elem_bytes && e.inner == inner && e.outer == outer && e.ld == ld &&
+        e.bi == box_inner && e.bo == box_outer) {
+      *map = e.map;
+      return true;
+    }
+  if (!make_map_plain_2d(map, ptr, elem_bytes, inner, outer, ld, box_inner, box_outer)) return false;
+  Entry& e = cache[next++ % 8];
+  e.ptr = ptr;
+  e.eb = elem_bytes;
   e.inner = inner;
   e.outer = outer;
   e.ld = ld;

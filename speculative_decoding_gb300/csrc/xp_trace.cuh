@@ -33,6 +33,13 @@ __device__ __forceinline__ void trace_mark(int slot) {
 }  // namespace xp
 
 #define XP_TRACE_MARK(slot) ::xp::trace_mark(slot)
+// record the SM this CTA runs on in `slot` (instead of a time)
+#define XP_TRACE_SM(slot)                                                              \
+  do {                                                                                 \
+    unsigned int sm_;                                                                  \
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm_));                                   \
+    if (blockIdx.x < (unsigned)::xp::kTraceCtas) ::xp::g_trace[blockIdx.x * ::xp::kTraceSlots + (slot)] = sm_ + 1; \
+  } while (0)
 // extern "C" int name(void* host, size_t bytes): copy the stamps out, then zero them
 #define XP_TRACE_READER(name)                                                              \
   extern "C" __attribute__((visibility("default"))) int name(void* host, size_t bytes) {   \
@@ -43,5 +50,6 @@ __device__ __forceinline__ void trace_mark(int slot) {
   }
 #else
 #define XP_TRACE_MARK(slot) ((void)0)
+#define XP_TRACE_SM(slot) ((void)0)
 #define XP_TRACE_READER(name)
 #endif
