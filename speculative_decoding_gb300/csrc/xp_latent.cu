@@ -901,13 +901,17 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     p.N = (int32_t)N;
     p.B = (int32_t)B;
     p.R = (int32_t)R;
-    p.tn = tn;
+    // 64-channel tiles and a 4-way H split: half the cluster reduction
+    // (distributed shared memory is the slow part here) for 1.5x the operand
+    // bytes per CTA; one CTA per SM (clusters of 4 always fit the GPCs)
+    const int dtn = 64;
+    p.tn = dtn;
     p.chunks = (int32_t)(H / LT_BK);
-    p.S = pow2_floor(p.chunks, LT_MAX_S);
-    p.w = tn / p.S;
-    p.ntiles = ntiles;
-    const uint32_t stage_bytes = LT_A_CHUNK + (uint32_t)tn * LT_BK * 2;
-    const size_t red_bytes = (size_t)LT_BM * (tn + 4) * 4;
+    p.S = pow2_floor(p.chunks, 4);
+    p.w = dtn / p.S;
+    p.ntiles = (int32_t)((R + dtn - 1) / dtn);
+    const uint32_t stage_bytes = LT_A_CHUNK + (uint32_t)dtn * LT_BK * 2;
+    const size_t red_bytes = (size_t)LT_BM * (dtn + 4) * 4;
     auto region_of = [&](int st) {
       const size_t ring = (size_t)st * stage_bytes;
       return (ring > red_bytes ? ring : red_bytes + 1023) & ~size_t(1023);
@@ -916,7 +920,7 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     // us, then full/empty per stage, acc_full, aux_full and the TMEM slot
     auto total = [&](int st) { return 1024 + region_of(st) + us_bytes + 8 * (2 * st + 2) + 16; };
     const int per_cta = (p.chunks + p.S - 1) / p.S;
-    p.stages = pick_stages(stage_bytes, per_cta, total);
+    p.stages = per_cta < 6 ? (per_cta < 2 ? 2 : per_cta) : 6;
     p.region = (uint32_t)region_of(p.stages);
     p.bar_off = p.region + (uint32_t)us_bytes;
     const size_t smem = total(p.stages);
@@ -927,7 +931,7 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
         !cached_map_plain_2d(&mapU, u, 4, (uint64_t)R, (uint64_t)rows, (uint64_t)R, (uint32_t)p.w, LT_BM))
       return XP_ERR_LAUNCH;
     void* args[] = {&mapM, &mapWd, &mapU, &p};
-    if (launch_ex((const void*)mlp_down_kernel, dim3((unsigned)(mtiles * ntiles * p.S)), smem, stream, p.S, args) !=
+    if (launch_ex((const void*)mlp_down_kernel, dim3((unsigned)(mtiles * p.ntiles * p.S)), smem, stream, p.S, args) !=
         cudaSuccess)
       return XP_ERR_LAUNCH;
   }

@@ -81,25 +81,28 @@ struct ReadoutParams {
 };
 
 // One 32-column chunk of one row: acc (fp32) -> bias = bf16(acc);
-// s = bf16(base + bias); update the running (best, first column).
-__device__ __forceinline__ void ro_chunk(const uint32_t (&r)[32], const uint32_t (&bw)[16], int col0, int V,
-                                         bool all_valid, float& best, int& bidx) {
+// s = bf16(base + bias); update the running (best, first column).  Base
+// columns at or past V arrive as NaN (the base tensor map's out-of-range
+// fill), so their sums are NaN: max.bf16x2 ignores a NaN operand and a NaN
+// never equals the maximum, so padding columns can neither raise the maximum
+// nor be chosen (for an odd V the upper half of the last pair included).
+__device__ __forceinline__ void ro_chunk(const uint32_t (&r)[32], const uint32_t (&bw)[16], int col0,
+                                         float& best, int& bidx) {
   uint32_t s2[16];
   uint32_t m2 = 0xff80ff80u;
 #pragma unroll
   for (int q = 0; q < 16; ++q) {
     const uint32_t bias2 = f32x2_to_bf16x2(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]));
     s2[q] = bf16x2_add(bw[q], bias2);
-    if (all_valid || col0 + 2 * q < V) m2 = bf16x2_max(m2, s2[q]);
+    m2 = bf16x2_max(m2, s2[q]);
   }
   const float m = fmaxf(bf16lo_to_f32(m2), bf16hi_to_f32(m2));
   if (m > best || bidx < 0) {
     int cand = -1;
 #pragma unroll
     for (int q = 15; q >= 0; --q) {
-      const bool ok = all_valid || (col0 + 2 * q < V);
-      if (ok && bf16hi_to_f32(s2[q]) == m) cand = 2 * q + 1;
-      if (ok && bf16lo_to_f32(s2[q]) == m) cand = 2 * q;
+      if (bf16hi_to_f32(s2[q]) == m) cand = 2 * q + 1;
+      if (bf16lo_to_f32(s2[q]) == m) cand = 2 * q;
     }
     if (cand >= 0) {
       best = m;
@@ -385,7 +388,6 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       }
       tc_fence_after();
       if (!dead) {
-        const bool all_valid = n0 + 64 <= p.V;
         // this row of the base box for columns [n0, n0+64): 128 bytes, its
         // 16-byte chunks permuted by the 128-byte swizzle (chunk ^ row%8)
         const uint8_t* brow = sBase + (size_t)bb * RO_BASE_TILE + (size_t)h * RO_BASE_BOX + (size_t)rr * 128;
@@ -403,7 +405,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
             bw[4 * v + 3] = x.w;
           }
           tmem_ld_wait();
-          ro_chunk(r, bw, n0 + c * 32, p.V, all_valid, best, bidx);
+          ro_chunk(r, bw, n0 + c * 32, best, bidx);
         }
       }
       tc_fence_before();
@@ -508,7 +510,8 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
 
   CUtensorMap mapW2, mapBase, mapLat;
   if (!cached_map_bf16_2d(&mapW2, W2t, (uint64_t)R, (uint64_t)V, (uint64_t)R, 64, RO_HALF)) return XP_ERR_LAUNCH;
-  if (!cached_map_bf16_2d(&mapBase, base, (uint64_t)V, (uint64_t)rows, (uint64_t)ld_base, 64, RO_BM))
+  // base: columns past V read as NaN (see ro_chunk)
+  if (!cached_map_bf16_2d(&mapBase, base, (uint64_t)V, (uint64_t)rows, (uint64_t)ld_base, 64, RO_BM, true))
     return XP_ERR_LAUNCH;
   if (!cached_map_bf16_2d(&mapLat, lat, (uint64_t)R, (uint64_t)rows, (uint64_t)R, 64, RO_BM)) return XP_ERR_LAUNCH;
 

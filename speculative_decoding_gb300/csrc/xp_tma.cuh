@@ -25,9 +25,10 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // 2-D bf16 tensor [outer, inner] with row pitch `ld` elements; box
 // [box_outer, box_inner] with 128-byte swizzle (box_inner * 2 must be 128).
-// Out-of-range elements of a box are filled with zeros.
+// Out-of-range elements of a box are filled with zeros, or with NaN when
+// nan_fill is set.
 inline bool make_map_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
-                             uint32_t box_inner, uint32_t box_outer) {
+                             uint32_t box_inner, uint32_t box_outer, bool nan_fill = false) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -36,7 +37,7 @@ inline bool make_map_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner, 
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   nan_fill ? CU_TENSOR_MAP_FLOAT_OOB_FILL_NAN_REQUEST_ZERO_FMA : CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -61,24 +62,26 @@ inline bool make_map_plain_2d(CUtensorMap* map, const void* ptr, uint32_t elem_b
 // make_map_bf16_2d through a small per-thread cache keyed on every argument,
 // so repeated calls on the same buffers skip the encode.
 inline bool cached_map_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
-                               uint32_t box_inner, uint32_t box_outer) {
+                               uint32_t box_inner, uint32_t box_outer, bool nan_fill = false) {
   struct Entry {
     const void* ptr;
     uint64_t inner, outer, ld;
     uint32_t bi, bo;
+    bool nan;
     CUtensorMap map;
   };
   static thread_local Entry cache[16];
   static thread_local unsigned next = 0;
   for (auto& e : cache)
     if (e.ptr == ptr && e.inner == inner && e.outer == outer && e.ld == ld && e.bi == box_inner &&
-        e.bo == box_outer) {
+        e.bo == box_outer && e.nan == nan_fill) {
       *map = e.map;
       return true;
     }
-  if (!make_map_bf16_2d(map, ptr, inner, outer, ld, box_inner, box_outer)) return false;
+  if (!make_map_bf16_2d(map, ptr, inner, outer, ld, box_inner, box_outer, nan_fill)) return false;
   Entry& e = cache[next++ % 16];
   e.ptr = ptr;
+  e.nan = nan_fill;
   e.inner = inner;
   e.outer = outer;
   e.ld = ld;

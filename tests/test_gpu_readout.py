@@ -70,6 +70,24 @@ def test_exact_inputs_bit_exact(orc, N, B, V, R):
     assert changed == int((want != blk).sum())
 
 
+@pytest.mark.parametrize("N,B,V,R", [(3, 5, 1001, 64), (2, 3, 33, 32), (4, 9, 4097, 128)])
+def test_odd_vocab_all_negative(orc, N, B, V, R):
+    """V odd, and V < 64 (a whole 32-column chunk of the first tile lies past
+    V): the padding past V reads as zero on the device, which would beat
+    every real logit here (all negative); it must never win.  The base rows
+    need a leading dimension that is a multiple of 8."""
+    rows = N * (B - 1)
+    lat, W2, base = _exact_inputs(rows, V, R, seed=V)
+    base = _bits(synth._f32(base) - 64.0)
+    blk = synth.tokens(8, 8, (N, B), V)
+    got, changed = _run(lat, W2, base, blk, ld=(V + 7) // 8 * 8)
+    bias = orc.readout_bias(lat, W2)
+    want = blk.copy()
+    orc.add_argmax(base, bias, want)
+    np.testing.assert_array_equal(got, want)
+    assert changed == int((want != blk).sum())
+
+
 def test_exact_inputs_strided_base(orc):
     N, B, V, R = 3, 5, 1000, 64
     rows = N * (B - 1)
