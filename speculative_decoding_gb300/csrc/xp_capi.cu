@@ -130,9 +130,8 @@ xp_status check_latent_args(const int64_t* blk, const int64_t* am1, const xp_bf1
 extern "C" {
 
 size_t xp_latent_workspace_size(int64_t N, int64_t B, int64_t D, int64_t R, int64_t H) {
-  (void)D;
-  if (N < 0 || B < 2 || R < 0 || H < 0) return 0;
-  return xp::latent_ws_layout(N, B, R, H).total_latent;
+  if (N < 0 || B < 2 || D < 0 || R < 0 || H < 0) return 0;
+  return xp::latent_ws_layout(N, B, D, R, H).total_latent;
 }
 
 xp_status xp_latent_pass(const int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_hcache, const xp_bf16* d_E,
@@ -143,7 +142,7 @@ xp_status xp_latent_pass(const int64_t* d_blk, const int64_t* d_am1, const xp_bf
   if (st != XP_OK || N == 0) return st;
   if (!d_lat_out || !d_workspace) return XP_ERR_NULL;
   if (!aligned16(d_lat_out)) return XP_ERR_ALIGN;
-  if (!aligned256(d_workspace) || workspace_bytes < xp::latent_ws_layout(N, B, R, H).total_latent)
+  if (!aligned256(d_workspace) || workspace_bytes < xp::latent_ws_layout(N, B, D, R, H).total_latent)
     return XP_ERR_WORKSPACE;
   st = check_device();
   if (st != XP_OK) return st;
@@ -153,9 +152,8 @@ xp_status xp_latent_pass(const int64_t* d_blk, const int64_t* d_am1, const xp_bf
 
 size_t xp_jacobi_workspace_size(int64_t N, int64_t B, int64_t V, int64_t D, int64_t R, int64_t H) {
   (void)V;
-  (void)D;
-  if (N < 0 || B < 2 || R < 0 || H < 0) return 0;
-  return xp::latent_ws_layout(N, B, R, H).total_pass;
+  if (N < 0 || B < 2 || D < 0 || R < 0 || H < 0) return 0;
+  return xp::latent_ws_layout(N, B, D, R, H).total_pass;
 }
 
 xp_status xp_jacobi_pass(int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_hcache, const xp_bf16* d_E,
@@ -168,7 +166,7 @@ xp_status xp_jacobi_pass(int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_
   if (ld_base < V) return XP_ERR_SHAPE;
   if (!d_W2t || !d_base || !d_workspace) return XP_ERR_NULL;
   if (!aligned16(d_W2t) || !aligned16(d_base) || (ld_base & 7) || ((uintptr_t)d_changed & 3)) return XP_ERR_ALIGN;
-  const xp::LatentWsLayout lay = xp::latent_ws_layout(N, B, R, H);
+  const xp::LatentWsLayout lay = xp::latent_ws_layout(N, B, D, R, H);
   if (!aligned256(d_workspace) || workspace_bytes < lay.total_pass) return XP_ERR_WORKSPACE;
   st = check_device();
   if (st != XP_OK) return st;

@@ -105,16 +105,44 @@ __host__ inline ArgmaxWs argmax_ws(void* ws, int64_t rows) {
   return w;
 }
 
-// Latent / full-pass workspace: the argmax part for rows = N*(B-1), then
-//   u   fp32 [N*B, R]   mixer output (the MLP residual)
-//   ub  bf16 [N*B, R]   bf16(u), the MLP input
-//   m   bf16 [N*B, H]   bf16(silu(ub@Wg) * (ub@Wu))
-//   lat bf16 [N*(B-1), R]  the latent read by the readout (full pass only)
-struct LatentWsLayout {
-  size_t u, ub, m, lat, total_latent, total_pass;
+// Tiling of the latent stage's projection x = E[prev] @ W_lat (shared by the
+// kernel launch and the workspace layout): M tiles of bpt whole blocks
+// (<= 128 rows), N tiles of tn latent channels, the D-long reduction split
+// S ways; each split writes an fp32 partial tile that the S CTAs of the tile
+// then sum in a fixed order.
+struct ProjTiling {
+  int32_t bpt, mtiles, tn, ntiles, chunks, S, w;
+  int64_t rows_pad, r_pad;  // partial-sum buffer: [S][rows_pad][r_pad] fp32
 };
-__host__ inline LatentWsLayout latent_ws_layout(int64_t N, int64_t B, int64_t R, int64_t H) {
+__host__ inline ProjTiling proj_tiling(int64_t N, int64_t B, int64_t D, int64_t R) {
+  ProjTiling t;
+  t.bpt = B <= 128 ? (int32_t)(128 / B) : 1;
+  t.mtiles = (int32_t)((N + t.bpt - 1) / t.bpt);
+  t.tn = R >= 128 ? 128 : 64;
+  t.ntiles = (int32_t)((R + t.tn - 1) / t.tn);
+  t.chunks = (int32_t)((D + 63) / 64);
+  t.S = 1;
+  while (t.S * 2 <= t.chunks && t.S * 2 <= 8) t.S *= 2;
+  t.w = t.tn / t.S;
+  t.rows_pad = (int64_t)t.mtiles * 128;
+  t.r_pad = (int64_t)t.ntiles * t.tn;
+  return t;
+}
+
+// Latent / full-pass workspace: the argmax part for rows = N*(B-1), then
+//   u    fp32 [N*B, R]   mixer output (the MLP residual)
+//   ub   bf16 [N*B, R]   bf16(u), the MLP input
+//   m    bf16 [N*B, H]   bf16(silu(ub@Wg) * (ub@Wu))
+//   part fp32 [S, rows_pad, r_pad]  the projection's partial sums
+//   cnt  u32  [mtiles * ntiles, 2]  per projection tile: partials written,
+//                                   partials read (zero between calls)
+//   lat  bf16 [N*(B-1), R]  the latent read by the readout (full pass only)
+struct LatentWsLayout {
+  size_t u, ub, m, part, cnt, lat, total_latent, total_pass;
+};
+__host__ inline LatentWsLayout latent_ws_layout(int64_t N, int64_t B, int64_t D, int64_t R, int64_t H) {
   LatentWsLayout L;
+  const ProjTiling t = proj_tiling(N, B, D, R);
   size_t off = argmax_ws_bytes(N * (B - 1));
   L.u = off;
   off += align256(4 * (size_t)(N * B * R));
@@ -122,6 +150,10 @@ __host__ inline LatentWsLayout latent_ws_layout(int64_t N, int64_t B, int64_t R,
   off += align256(2 * (size_t)(N * B * R));
   L.m = off;
   off += align256(2 * (size_t)(N * B * H));
+  L.part = off;
+  off += align256(4 * (size_t)t.S * (size_t)t.rows_pad * (size_t)t.r_pad);
+  L.cnt = off;
+  off += align256(8 * (size_t)t.mtiles * (size_t)t.ntiles);
   L.total_latent = off;
   L.lat = off;
   off += align256(2 * (size_t)(N * (B - 1) * R));

@@ -52,12 +52,17 @@ __device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float((uint
 // proj_mix: x = hcache + E[prev] @ W_lat, then the causal mixer
 // ============================================================================
 // Shared memory: [0, region) is the stage ring; once the MMAs are done it holds
-// red[128][tn + 4] (this CTA's fp32 partial sums, read by the whole cluster)
-// and xs[128][w] (the reduced x of this CTA's w columns).  After it: Ls (the
-// mixer weights of those columns, lower triangle packed by rows), hcs (the
-// hidden cache of those columns for the tile's 128 rows), the token table and
-// the barriers.  Ls and hcs are copied by the bulk-copy engine at the start,
-// while the reduction runs, so the epilogue reads neither from global memory.
+// the S partial-sum slices of this CTA's w columns (TMA from the partial
+// buffer) and xs[128][w] (the reduced x).  After it: Ls (the mixer weights of
+// those columns, lower triangle packed by rows), hcs (the hidden cache of
+// those columns for the tile's 128 rows), the token table and the barriers.
+//
+// The S CTAs of a tile (one per slice of the D-long reduction) are ordinary
+// CTAs, not a cluster: each writes its fp32 partial tile to the partial
+// buffer (L2-resident), counts itself on the tile's arrival counter, waits
+// (bounded) until all S have arrived, then loads the S partials of its own w
+// columns and sums them in slice order.  The grid is one wave (one CTA per
+// SM), so every CTA a wait depends on is resident.
 struct ProjParams {
   const int64_t* blk;
   const int64_t* am1;
@@ -65,8 +70,11 @@ struct ProjParams {
   const float* L;
   float* u;
   uint16_t* ub;
+  float* part;
+  uint32_t* cnt;
   WsHeader* hdr;
   int32_t N, B, V, D, R, bpt, tn, S, w, chunks, ntiles, stages;
+  int64_t rows_pad, r_pad;
   uint32_t region, hc_off, tok_off, bar_off;
 };
 
@@ -74,8 +82,9 @@ __host__ __device__ inline uint32_t proj_ls_bytes(int B, int w) {
   return (uint32_t)(((B * (B + 1) / 2) * w * 4 + 127) & ~127);
 }
 
-__global__ void __launch_bounds__(LT_THREADS, 2)
+__global__ void __launch_bounds__(LT_THREADS, 1)
 proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_constant__ CUtensorMap mapHc,
+                const __grid_constant__ CUtensorMap mapPart, const __grid_constant__ CUtensorMap mapPartSt,
                 const ProjParams p) {
   extern __shared__ uint8_t smem_raw[];
   if (threadIdx.x == 0) XP_TRACE_MARK(0);
@@ -83,22 +92,26 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
   uint8_t* smem = align1024(smem_raw);
   const uint32_t b_bytes = (uint32_t)p.tn * LT_BK * 2;
   const uint32_t stage_bytes = LT_A_CHUNK + b_bytes;
-  const int ld = p.tn + 4;  // floats per row of red (a 16-byte multiple)
-  float* red = reinterpret_cast<float*>(smem);
-  float* xs = red + LT_BM * ld;
+  float* slices = reinterpret_cast<float*>(smem);     // [S][128][w]
+  float* xs = slices + (size_t)p.S * LT_BM * p.w;     // [128][w]
+  // this CTA's partial tile on its way out: tn/32 boxes of [128][32] fp32,
+  // 128-byte swizzled (1024-byte aligned, after slices and xs)
+  uint8_t* pst = smem + (((size_t)(p.S + 1) * LT_BM * p.w * 4 + 1023) & ~size_t(1023));
   float* Ls = reinterpret_cast<float*>(smem + p.region);
   const uint16_t* hcs = reinterpret_cast<const uint16_t*>(smem + p.hc_off);
   int64_t* tok = reinterpret_cast<int64_t*>(smem + p.tok_off);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
   uint64_t* empty = full + p.stages;
   uint64_t* acc_full = empty + p.stages;
-  uint64_t* aux_full = acc_full + 1;  // Ls and hcs landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_full + 1);
+  uint64_t* aux_full = acc_full + 1;    // Ls and hcs landed
+  uint64_t* slice_full = aux_full + 1;  // the S partial slices landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(slice_full + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ks = (int)(blockIdx.x % p.S);
   const int nt = (int)((blockIdx.x / p.S) % p.ntiles);
   const int mt = (int)(blockIdx.x / (p.S * p.ntiles));
+  const int tile = mt * p.ntiles + nt;
   const int c0 = (int)((int64_t)ks * p.chunks / p.S);
   const int nck = (int)((int64_t)(ks + 1) * p.chunks / p.S) - c0;
   const int c_lo = ks * p.w;                   // this CTA's columns of the tile: [c_lo, c_lo + w)
@@ -115,6 +128,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     }
     mbar_init(acc_full, 1);
     mbar_init(aux_full, 1);
+    mbar_init(slice_full, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -130,14 +144,14 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
 
   if (warp == 0) {
     // Nothing this warp reads is written by the preceding kernels, so it
-    // starts before the dependency wait: the mixer weights (one bulk copy
-    // per (b, j) pair of the lower triangle: the slice's wv channels), the
-    // hidden-cache slice (one tensor box), then the W_lat ring.  Lane 0
-    // waits for a stage and arms its barrier; lanes 0..tn/64-1 issue one
-    // W_lat box each (a single thread issues tiled copies slowly).
+    // starts before the dependency wait: the W_lat ring, then the hidden-cache
+    // slice (one tensor box) and the mixer weights (one bulk copy per (b, j)
+    // pair of the lower triangle: the slice's wv channels).  The copy engine
+    // serves requests in order, so the epilogue's operands (needed only after
+    // the MMAs) go after the first W_lat stages.  Lane 0 waits for a stage and
+    // arms its barrier; lanes 0..tn/64-1 issue one W_lat box each (a single
+    // thread issues tiled copies slowly).
     const int tri = p.B * (p.B + 1) / 2;
-    // the copy engine serves requests in order: the first W_lat stages go
-    // first, the epilogue's operands (needed only after the MMAs) after them
     auto aux_copies = [&]() {
       if (lane == 0) {
         mbar_arrive_expect_tx(aux_full, (uint32_t)(tri * wv * 4) + (uint32_t)(LT_BM * p.w * 2));
@@ -157,10 +171,8 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     if (lane == 0) {
       prefetch_tensormap(&mapWlat);
       prefetch_tensormap(&mapHc);
+      prefetch_tensormap(&mapPart);
     }
-    // the W_lat boxes beyond the ring's first round: into L2 now
-    for (int i = p.stages + lane / (p.tn / 64); i < nck; i += 32 / (p.tn / 64))
-      tma_prefetch_2d(&mapWlat, nt * p.tn + (lane % (p.tn / 64)) * 64, (c0 + i) * LT_BK);
     for (int i = 0; i < nck; ++i) {
       if (i == p.stages) aux_copies();
       const uint32_t s = i % p.stages, k = i / p.stages;
@@ -229,7 +241,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     // one 128-byte row piece, so each copy instruction reads four whole
     // rows; a stage's copies form one cp.async group, and a warp hands a
     // stage over (wait for its group, proxy fence, arrive) only when it is
-    // LAG stages ahead, so up to LAG + 1 stages per warp are in flight.
+    // LAG = stages - 1 stages ahead, so the whole ring is in flight.
     const int gw = warp - 2, rsub = lane >> 3, piece = lane & 7;
     bool dead = false;
     auto hand_over = [&](int i) {
@@ -239,7 +251,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
       if (lane == 0 && i == 0) XP_TRACE_MARK(5);
       if (lane == 0 && i == nck - 1) XP_TRACE_MARK(6);
     };
-    const int lag = p.stages - 1;  // 1 or 2 (stages is 2 or 3)
+    const int lag = p.stages - 1;  // 1..5
     for (int i = 0; i < nck; ++i) {
       const int s = i % p.stages, k = i / p.stages;
       if (k >= 1 && !mbar_wait(&empty[s], (k - 1) & 1)) {
@@ -258,8 +270,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
       }
       cp_async_commit();
       if (i >= lag) {
-        if (lag == 2) cp_async_wait_group<2>();
-        else cp_async_wait_group<1>();
+        cp_async_wait_group_n(lag);
         hand_over(i - lag);
       }
     }
@@ -272,7 +283,9 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     }
   }
 
-  // ---- epilogue 1: the partial sums TMEM -> red (warps 2..5, one row each)
+  // ---- epilogue 1: this CTA's fp32 partial tile TMEM -> shared memory (one
+  // row per thread, 128-byte swizzle: conflict-free) -> TMA stores into the
+  // partial buffer
   if (warp >= 2) {
     if (!mbar_wait(acc_full, 0)) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
     tc_fence_after();
@@ -282,63 +295,87 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
       uint32_t r[32];
       tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + c * 32, r);
       tmem_ld_wait();
-      float4* dst = reinterpret_cast<float4*>(red + row * ld + c * 32);
+      uint8_t* box = pst + (size_t)c * (LT_BM * 128) + (size_t)row * 128;
 #pragma unroll
       for (int e = 0; e < 8; ++e)
-        dst[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]), __uint_as_float(r[4 * e + 2]),
-                             __uint_as_float(r[4 * e + 3]));
+        *reinterpret_cast<uint4*>(box + ((e ^ (row & 7)) << 4)) = make_uint4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
+    }
+    fence_proxy_async_smem();
+    named_barrier_sync(1, 128);
+    if (threadIdx.x == 64) {
+      for (int c = 0; c < p.tn / 32; ++c)
+        tma_store_2d(&mapPartSt, pst + (size_t)c * (LT_BM * 128), nt * p.tn + c * 32,
+                     (int)((int64_t)ks * p.rows_pad + (int64_t)mt * LT_BM));
+      bulk_commit();
+      bulk_wait_all();  // the partial tile is in global memory
+      XP_TRACE_MARK(10);
     }
   }
-  if (threadIdx.x == 64) XP_TRACE_MARK(10);
   tc_fence_before();
-  cluster_sync();
+  __syncthreads();  // the partial tile of this CTA is stored
+  if (warp == 0) {
+    // publish this CTA's partial, wait for the other S-1, then fetch the S
+    // partials of this CTA's w columns (one TMA box each, lanes in parallel)
+    int ok = 1;
+    if (lane == 0) {
+      fence_proxy_async_global();
+      __threadfence();
+      atomicAdd(&p.cnt[2 * tile], 1u);
+      const unsigned long long t0 = globaltimer();
+      while (ld_acquire_gpu(&p.cnt[2 * tile]) < (uint32_t)p.S) {
+        if (globaltimer() - t0 > kWaitLimitNs) {
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+      fence_proxy_async_global();
+      if (ok) mbar_arrive_expect_tx(slice_full, (uint32_t)(p.S * LT_BM * p.w * 4));
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      if (lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+    } else {
+      if (lane < p.S)
+        tma_load_2d(slices + (size_t)lane * LT_BM * p.w, &mapPart, col0,
+                    (int)((int64_t)lane * p.rows_pad + (int64_t)mt * LT_BM), slice_full);
+      // once the slices are here this CTA is done with the partial buffer:
+      // the last of the S to get there resets the tile's counters
+      if (lane == 0 && mbar_wait(slice_full, 0)) {
+        if (atomicAdd(&p.cnt[2 * tile + 1], 1u) == (uint32_t)p.S - 1) {
+          p.cnt[2 * tile] = 0u;
+          p.cnt[2 * tile + 1] = 0u;
+        }
+      }
+    }
+    if (lane == 0) XP_TRACE_MARK(11);
+  }
 
   if (warp >= 2) {
     const int et = threadIdx.x - 64;
-    if (et == 0) XP_TRACE_MARK(11);
-    if (!mbar_wait(aux_full, 0)) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
-    // ---- epilogue 2: x = hcache + sum of the cluster's partials (fixed
-    // order) for this CTA's columns of all rows; two (row, 4 columns) items
-    // per thread per round, every partial requested before any is used
+    if (!mbar_wait(slice_full, 0) || !mbar_wait(aux_full, 0)) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+    // ---- epilogue 2: x = hcache + sum of the S partials (slice order) for
+    // this CTA's columns of all rows, four columns per item
     const int wq = p.w / 4, items = LT_BM * wq;
-    for (int i0 = et; i0 < items; i0 += 256) {
-      float4 v[2][LT_MAX_S];
-      int rr[2], gg[2];
-      bool on[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int it = i0 + h * 128;
-        rr[h] = it / wq;
-        gg[h] = it - rr[h] * wq;
-        const int bl = rr[h] / p.B;
-        on[h] = it < items && bl < nbl;
-#pragma unroll
-        for (int q = 0; q < LT_MAX_S; ++q)
-          v[h][q] = (on[h] && q < p.S) ? ld_dsmem_v4(red + rr[h] * ld + c_lo + 4 * gg[h], (uint32_t)q)
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int it = et; it < items; it += 128) {
+      const int rr = it / wq, gg = it - rr * wq;
+      if (rr / p.B >= nbl) continue;
+      float4 a = *reinterpret_cast<const float4*>(slices + rr * p.w + 4 * gg);
+      for (int q = 1; q < p.S; ++q) {
+        const float4 v = *reinterpret_cast<const float4*>(slices + ((size_t)q * LT_BM + rr) * p.w + 4 * gg);
+        a.x += v.x;
+        a.y += v.y;
+        a.z += v.z;
+        a.w += v.w;
       }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (!on[h]) continue;
-        float4 a = v[h][0];
-#pragma unroll
-        for (int q = 1; q < LT_MAX_S; ++q) {
-          if (q < p.S) {
-            a.x += v[h][q].x;
-            a.y += v[h][q].y;
-            a.z += v[h][q].z;
-            a.w += v[h][q].w;
-          }
-        }
-        // the hidden cache of these 4 channels (zero past R: TMA fill)
-        const uint2 hc = *reinterpret_cast<const uint2*>(hcs + rr[h] * p.w + 4 * gg[h]);
-        float4 x;
-        x.x = bf16lo_to_f32(hc.x) + a.x;
-        x.y = bf16hi_to_f32(hc.x) + a.y;
-        x.z = bf16lo_to_f32(hc.y) + a.z;
-        x.w = bf16hi_to_f32(hc.y) + a.w;
-        *reinterpret_cast<float4*>(xs + rr[h] * p.w + 4 * gg[h]) = x;
-      }
+      // the hidden cache of these 4 channels (zero past R: TMA fill)
+      const uint2 hc = *reinterpret_cast<const uint2*>(hcs + rr * p.w + 4 * gg);
+      float4 x;
+      x.x = bf16lo_to_f32(hc.x) + a.x;
+      x.y = bf16hi_to_f32(hc.x) + a.y;
+      x.z = bf16lo_to_f32(hc.y) + a.z;
+      x.w = bf16hi_to_f32(hc.y) + a.w;
+      *reinterpret_cast<float4*>(xs + rr * p.w + 4 * gg) = x;
     }
     if (et == 127) XP_TRACE_MARK(12);
     named_barrier_sync(1, 128);
@@ -366,7 +403,8 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     }
     if (et == 0) XP_TRACE_MARK(13);
   }
-  cluster_sync_relaxed();  // the peers have finished reading this CTA's partial sums
+  tc_fence_before();
+  __syncthreads();
   if (threadIdx.x == 0) XP_TRACE_MARK(14);
   if (warp == 1) {
     tc_fence_after();
@@ -766,27 +804,7 @@ int pow2_floor(int x, int cap) {
   return s;
 }
 
-// Dynamic shared memory that still lets two CTAs share an SM: 228 KB per SM,
-// 1 KB of it reserved per CTA, with some margin.
-constexpr size_t kTwoPerSm = 112 * 1024;
-
-// Stage count for a ring of `stage_bytes` stages: deep enough for the CTA's
-// chunks (at most 6), then cut back (not below 2) until `total(stages)` fits
-// two CTAs per SM.
-template <class F>
-int pick_stages(uint32_t stage_bytes, int chunks_per_cta, F total) {
-  int st = chunks_per_cta < 6 ? chunks_per_cta : 6;
-  if (st < 2) st = 2;
-  while (st > 2 && total(st) > kTwoPerSm) --st;
-  (void)stage_bytes;
-  return st;
-}
-
 }  // namespace
-
-// The latent's tile width over R: 128 channels, or R rounded up to 64 when R
-// is smaller (the TMA zero-fills the missing weight columns).
-static int latent_tn(int64_t R) { return R >= 128 ? 128 : 64; }
 
 xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* hcache, const uint16_t* E,
                         const uint16_t* W_lat, const float* L, const uint16_t* Wg, const uint16_t* Wu,
@@ -810,18 +828,17 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
       return XP_ERR_LAUNCH;
     g_lt_attr[dev] = true;
   }
-  const LatentWsLayout lay = latent_ws_layout(N, B, R, H);
+  const LatentWsLayout lay = latent_ws_layout(N, B, D, R, H);
   char* w = static_cast<char*>(ws);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(w);
   float* u = reinterpret_cast<float*>(w + lay.u);
   uint16_t* ub = reinterpret_cast<uint16_t*>(w + lay.ub);
   uint16_t* m = reinterpret_cast<uint16_t*>(w + lay.m);
-  const int tn = latent_tn(R);
-  const int ntiles = (int)((R + tn - 1) / tn);
   const int rows = (int)(N * B);
 
   // ---- proj_mix
   {
+    const ProjTiling t = proj_tiling(N, B, D, R);
     ProjParams p;
     p.blk = blk;
     p.am1 = am1;
@@ -829,45 +846,50 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     p.L = L;
     p.u = u;
     p.ub = ub;
+    p.part = reinterpret_cast<float*>(w + lay.part);
+    p.cnt = reinterpret_cast<uint32_t*>(w + lay.cnt);
     p.hdr = hdr;
     p.N = (int32_t)N;
     p.B = (int32_t)B;
     p.V = (int32_t)V;
     p.D = (int32_t)D;
     p.R = (int32_t)R;
-    p.bpt = (int32_t)(LT_BM / B);
-    p.tn = tn;
-    p.chunks = (int32_t)((D + LT_BK - 1) / LT_BK);
-    p.S = pow2_floor(p.chunks, LT_MAX_S);
-    p.w = tn / p.S;
-    p.ntiles = ntiles;
-    const uint32_t stage_bytes = LT_A_CHUNK + (uint32_t)tn * LT_BK * 2;
-    const size_t red_xs = (size_t)LT_BM * (tn + 4) * 4 + (size_t)LT_BM * p.w * 4;
-    const size_t ls = proj_ls_bytes((int)B, p.w);
-    const size_t hc = ((size_t)LT_BM * p.w * 2 + 127) & ~size_t(127);
-    auto region_of = [&](int st) {
-      const size_t ring = (size_t)st * stage_bytes;
-      return (ring > red_xs ? ring : red_xs + 1023) & ~size_t(1023);
-    };
-    // Ls, hcs, the token table, then full/empty per stage, acc_full,
-    // aux_full and the TMEM address slot
-    auto total = [&](int st) { return 1024 + region_of(st) + ls + hc + 8 * LT_BM + 8 * (2 * st + 2) + 16; };
-    // the gathering warps keep stages - 1 stages in flight: 2 or 3 stages
-    const int per_cta = (p.chunks + p.S - 1) / p.S;
-    p.stages = per_cta >= 3 ? 3 : 2;
-    if (p.stages == 3 && total(3) > kTwoPerSm) p.stages = 2;
-    p.region = (uint32_t)region_of(p.stages);
+    p.bpt = t.bpt;
+    p.tn = t.tn;
+    p.chunks = t.chunks;
+    p.S = t.S;
+    p.w = t.w;
+    p.ntiles = t.ntiles;
+    p.rows_pad = t.rows_pad;
+    p.r_pad = t.r_pad;
+    const uint32_t stage_bytes = LT_A_CHUNK + (uint32_t)t.tn * LT_BK * 2;
+    // after the MMAs the ring holds the S partial slices, xs and (1024-byte
+    // aligned) the outgoing partial tile
+    const size_t sl_xs =
+        (((size_t)(t.S + 1) * LT_BM * t.w * 4 + 1023) & ~size_t(1023)) + (size_t)LT_BM * t.tn * 4;
+    const size_t ls = proj_ls_bytes((int)B, t.w);
+    const size_t hc = ((size_t)LT_BM * t.w * 2 + 127) & ~size_t(127);
+    // the gathering warps keep stages - 1 stages in flight
+    const int per_cta = (t.chunks + t.S - 1) / t.S;
+    p.stages = per_cta < 6 ? (per_cta < 2 ? 2 : per_cta) : 6;
+    const size_t ring = (size_t)p.stages * stage_bytes;
+    p.region = (uint32_t)((ring > sl_xs ? ring : sl_xs + 1023) & ~size_t(1023));
     p.hc_off = p.region + (uint32_t)ls;
     p.tok_off = p.hc_off + (uint32_t)hc;
     p.bar_off = p.tok_off + 8 * LT_BM;
-    const size_t smem = total(p.stages);
-    const int mtiles = (int)((N + p.bpt - 1) / p.bpt);
-    CUtensorMap mapWlat, mapHc;
+    // Ls, hcs, the token table, then full/empty per stage, acc_full,
+    // aux_full, slice_full and the TMEM address slot
+    const size_t smem = 1024 + (size_t)p.bar_off + 8 * (2 * p.stages + 3) + 16;
+    CUtensorMap mapWlat, mapHc, mapPart, mapPartSt;
     if (!cached_map_bf16_2d(&mapWlat, W_lat, (uint64_t)R, (uint64_t)D, (uint64_t)R, 64, LT_BK) ||
-        !cached_map_plain_2d(&mapHc, hcache, 2, (uint64_t)R, (uint64_t)(N * B), (uint64_t)R, (uint32_t)p.w, LT_BM))
+        !cached_map_plain_2d(&mapHc, hcache, 2, (uint64_t)R, (uint64_t)(N * B), (uint64_t)R, (uint32_t)t.w, LT_BM) ||
+        !cached_map_plain_2d(&mapPart, p.part, 4, (uint64_t)t.r_pad, (uint64_t)(t.S * t.rows_pad), (uint64_t)t.r_pad,
+                             (uint32_t)t.w, LT_BM) ||
+        !cached_map_plain_2d(&mapPartSt, p.part, 4, (uint64_t)t.r_pad, (uint64_t)(t.S * t.rows_pad),
+                             (uint64_t)t.r_pad, 32, LT_BM, true))
       return XP_ERR_LAUNCH;
-    void* args[] = {&mapWlat, &mapHc, &p};
-    if (launch_ex((const void*)proj_mix_kernel, dim3((unsigned)(mtiles * ntiles * p.S)), smem, stream, p.S, args) !=
+    void* args[] = {&mapWlat, &mapHc, &mapPart, &mapPartSt, &p};
+    if (launch_ex((const void*)proj_mix_kernel, dim3((unsigned)(t.mtiles * t.ntiles * t.S)), smem, stream, 1, args) !=
         cudaSuccess)
       return XP_ERR_LAUNCH;
   }

@@ -44,9 +44,10 @@ inline bool make_map_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner, 
 // 2-D tensor [outer, inner] of 2- or 4-byte elements (bf16 or fp32), row
 // pitch `ld` elements, box [box_outer, box_inner] without swizzle (the box
 // lands in shared memory as dense rows of box_inner elements; box_inner *
-// elem_bytes must be a multiple of 16).  Out-of-range elements read as zero.
+// elem_bytes must be a multiple of 16), or with the 128-byte swizzle
+// (box_inner * elem_bytes == 128).  Out-of-range elements read as zero.
 inline bool make_map_plain_2d(CUtensorMap* map, const void* ptr, uint32_t elem_bytes, uint64_t inner, uint64_t outer,
-                              uint64_t ld, uint32_t box_inner, uint32_t box_outer) {
+                              uint64_t ld, uint32_t box_inner, uint32_t box_outer, bool swizzle128 = false) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -55,7 +56,8 @@ inline bool make_map_plain_2d(CUtensorMap* map, const void* ptr, uint32_t elem_b
   cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUresult r = enc(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -93,24 +95,27 @@ inline bool cached_map_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner
 
 // make_map_plain_2d through its own small per-thread cache.
 inline bool cached_map_plain_2d(CUtensorMap* map, const void* ptr, uint32_t elem_bytes, uint64_t inner,
-                                uint64_t outer, uint64_t ld, uint32_t box_inner, uint32_t box_outer) {
+                                uint64_t outer, uint64_t ld, uint32_t box_inner, uint32_t box_outer,
+                                bool swizzle128 = false) {
   struct Entry {
     const void* ptr;
     uint64_t inner, outer, ld;
     uint32_t eb, bi, bo;
+    bool sw;
     CUtensorMap map;
   };
   static thread_local Entry cache[8];
   static thread_local unsigned next = 0;
   for (auto& e : cache)
     if (e.ptr == ptr && e.eb == elem_bytes && e.inner == inner && e.outer == outer && e.ld == ld &&
-        e.bi == box_inner && e.bo == box_outer) {
+        e.bi == box_inner && e.bo == box_outer && e.sw == swizzle128) {
       *map = e.map;
       return true;
     }
-  if (!make_map_plain_2d(map, ptr, elem_bytes, inner, outer, ld, box_inner, box_outer)) return false;
+  if (!make_map_plain_2d(map, ptr, elem_bytes, inner, outer, ld, box_inner, box_outer, swizzle128)) return false;
   Entry& e = cache[next++ % 8];
   e.ptr = ptr;
+  e.sw = swizzle128;
   e.eb = elem_bytes;
   e.inner = inner;
   e.outer = outer;
