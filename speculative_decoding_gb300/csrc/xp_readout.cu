@@ -68,6 +68,7 @@ constexpr int RO_SLOTS = 2;                            // slot t % 2 holds tile 
 constexpr uint32_t RO_BASE_BOX = RO_BM * 64 * 2;       // base box: 128 rows x 64 cols (16 KB)
 constexpr uint32_t RO_BASE_TILE = RO_BM * RO_BN * 2;   // 32 KB
 constexpr int RO_NBASE = 3;
+constexpr int RO_A_ROUND = 2 * RO_NBASE;                 // latent boxes per staging round (the base ring's 16 KB boxes)
 constexpr uint32_t RO_TMEM_A = 0;                      // A: columns [0, 32*kch)
 constexpr uint32_t RO_TMEM_ACC = 256;                  // accumulators: [256, 384), [384, 512)
 
@@ -148,11 +149,11 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
     for (int s = 0; s < RO_SLOTS; ++s) mbar_init(&b_full[s], 1);  // the leader's arrive_expect_tx (both halves)
     for (int s = 0; s < RO_NBASE; ++s) {
       mbar_init(&base_full[s], 1);
-      mbar_init(&base_empty[s], RO_EPI_WARPS);
+      mbar_init(&base_empty[s], 1);  // one arrive per CTA after the epilogue warps' barrier
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 2 * RO_EPI_WARPS);
+      mbar_init(&acc_empty[a], 2);  // one (release) arrive per CTA of the pair
     }
     mbar_init(a_ready, 2 * RO_EPI_WARPS);
     mbar_init(drain, 1);
@@ -222,9 +223,10 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   } else if (warp == RO_WARP_BASE) {
     // ---------------- TMA producer: base tiles (two lanes, one box each) ----------------
     // The latent tile (A) goes first, through the still-empty base ring:
-    // rounds of up to four 64-column boxes (64 KB), each copied to TMEM by
-    // the epilogue warps before the ring is reused.
-    const int rounds = (p.kch + 3) / 4;
+    // rounds of up to RO_A_ROUND 64-column boxes (the ring holds six 16 KB
+    // boxes), each round copied to TMEM by the epilogue warps before the ring
+    // is reused.
+    const int rounds = (p.kch + RO_A_ROUND - 1) / RO_A_ROUND;
     bool a_dead = false;
     const uint64_t pol_base = policy_evict_first();  // read once per pass
     if (lane == 0) {
@@ -236,7 +238,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       tma_prefetch_2d(&mapBase, (n_begin + lane / 2) * RO_BN + (lane & 1) * 64, m_tile * RO_BM);
     pdl_wait();
     for (int r = 0; r < rounds && !a_dead; ++r) {
-      const int nbox = p.kch - 4 * r < 4 ? p.kch - 4 * r : 4;
+      const int nbox = p.kch - RO_A_ROUND * r < RO_A_ROUND ? p.kch - RO_A_ROUND * r : RO_A_ROUND;
       int ok = 1;
       if (lane == 0) {
         if (r >= 1 && !mbar_wait(a_free, (r - 1) & 1)) ok = 0;
@@ -247,7 +249,8 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
         break;
       }
       if (lane < nbox)
-        tma_load_2d(sBase + (size_t)lane * RO_BASE_BOX, &mapLat, (4 * r + lane) * 64, m_tile * RO_BM, &a_full[r]);
+        tma_load_2d(sBase + (size_t)lane * RO_BASE_BOX, &mapLat, (RO_A_ROUND * r + lane) * 64, m_tile * RO_BM,
+                    &a_full[r]);
     }
     {
       int ok = 1;
@@ -332,10 +335,10 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
     // Stage the A operand (this row of the latent, zero-padded to 64*kch)
     // into TMEM columns [0, 32*kch).  The latent arrives by TMA in the base
     // ring, 128-byte swizzled (chunk c of row rr at (c ^ rr%8)*16), in rounds
-    // of four 64-column boxes; the two warps of a lane quadrant take two
-    // boxes each.
+    // of up to six 64-column boxes; the two warps of a lane quadrant take
+    // alternate boxes.
     {
-      const int rounds = (p.kch + 3) / 4;
+      const int rounds = (p.kch + RO_A_ROUND - 1) / RO_A_ROUND;
       bool ok = true;
       for (int r = 0; r < rounds; ++r) {
         if (ok && !mbar_wait(&a_full[r], 0)) {
@@ -344,8 +347,8 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
         }
         if (ok) {
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int box = 2 * h + j, kc = 4 * r + box;
+          for (int j = 0; j < RO_A_ROUND / 2; ++j) {
+            const int box = 2 * j + h, kc = RO_A_ROUND * r + box;
             if (kc < p.kch) {
               const uint8_t* src = sBase + (size_t)box * RO_BASE_BOX + (size_t)rr * 128;
               uint32_t v[32];
@@ -408,9 +411,12 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
           ro_chunk(r, bw, n0 + c * 32, best, bidx);
         }
       }
+      // the eight epilogue warps meet, then one thread releases the
+      // accumulator and the base slot: a cluster-scope release arrive costs
+      // a memory barrier, so one per CTA and tile instead of one per warp
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
+      named_barrier_sync(2, 32 * RO_EPI_WARPS);
+      if (threadIdx.x == 64) {
         arrive_leader(&acc_empty[a]);
         mbar_arrive(&base_empty[bb]);
       }
