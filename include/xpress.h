@@ -126,6 +126,25 @@ XP_API xp_status xp_add_argmax_noalloc(const xp_bf16* d_base, int64_t ld_base, c
                                 int64_t B, xp_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * xp_topc_argmax -- the argmax over a slot's C gathered candidates, written
+ * back as a vocab id.
+ * Pages: fused_topc_argmax_to_blk / _xpress_topc_argmax_to_blk_kernel.
+ *
+ *   for r in [0, rows):  n = r / (B-1), j = r % (B-1)
+ *     p* = min { p : s[r,p] = max_p' s[r,p'] },
+ *     s[r,p] = bf16_round_nearest_even(float(base_c[r*C+p]) + float(bias_c[r*C+p]))
+ *     blk[n*B + 1 + j] = cand[r*C + p*]
+ *
+ * d_base_c, d_bias_c: [rows, C] bf16, dense (2-byte aligned); d_cand:
+ * [rows, C] int64 vocab ids; d_blk: [N, B] int64 with rows == N*(B-1).
+ * C in [1, 2^30].  -0 and +0 compare equal; inputs must be finite.  No
+ * workspace; one launch; nothing but blk[:, 1:] is written.
+ * ---------------------------------------------------------------------- */
+XP_API xp_status xp_topc_argmax(const xp_bf16* d_base_c, const xp_bf16* d_bias_c, const int64_t* d_cand,
+                                int64_t rows, int64_t C, int64_t* d_blk, int64_t N, int64_t B,
+                                xp_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * xp_latent_pass -- the fused latent stage.
  * Pages: xpress_latent_pass / _xpress_latent_kernel (in-kernel MLP form).
  *
@@ -192,6 +211,30 @@ XP_API xp_status xp_jacobi_pass(int64_t* d_blk, const int64_t* d_am1, const xp_b
                          int64_t B, int64_t V, int64_t D, int64_t R, int64_t H,
                          int32_t* d_changed, void* d_workspace, size_t workspace_bytes,
                          xp_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * xp_jacobi_fixpoint -- Jacobi passes to the fixpoint, without a host
+ * round trip: up to max_passes passes of xp_jacobi_pass on blk in place,
+ * stopping after the first pass that changes no slot of blk (that pass is
+ * counted).  Each pass reads the blk the previous one wrote
+ * (_xpress_add_argmax_reduce_to_blk_kernel docstring).
+ *
+ * All max_passes passes are enqueued at once (4 launches each, plus two
+ * small memsets), so the call is a fixed sequence of stream work (capturable
+ * in a CUDA graph); the kernels of a pass enqueued after the fixpoint find the
+ * workspace's convergence flag set and exit at their first instruction.
+ * d_passes (device int32, required) receives the number of passes that ran;
+ * d_changed (nullable, device int32) is incremented by the slots each pass
+ * changed.  max_passes in [1, 1024].  Other arguments, constraints and the
+ * workspace (xp_jacobi_workspace_size) as for xp_jacobi_pass.
+ * ---------------------------------------------------------------------- */
+XP_API xp_status xp_jacobi_fixpoint(int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_hcache,
+                                    const xp_bf16* d_E, const xp_bf16* d_W_lat, const float* d_L,
+                                    const xp_bf16* d_Wg, const xp_bf16* d_Wu, const xp_bf16* d_Wd,
+                                    const xp_bf16* d_W2, const xp_bf16* d_base, int64_t ld_base, int64_t N,
+                                    int64_t B, int64_t V, int64_t D, int64_t R, int64_t H, int32_t max_passes,
+                                    int32_t* d_passes, int32_t* d_changed, void* d_workspace,
+                                    size_t workspace_bytes, xp_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * xp_read_error -- copy the workspace's device-side error bits (XP_DEVERR_*)

@@ -129,6 +129,18 @@ xp_status check_latent_args(const int64_t* blk, const int64_t* am1, const xp_bf1
 
 extern "C" {
 
+xp_status xp_topc_argmax(const xp_bf16* d_base_c, const xp_bf16* d_bias_c, const int64_t* d_cand, int64_t rows,
+                         int64_t C, int64_t* d_blk, int64_t N, int64_t B, xp_stream_t stream) {
+  if (N < 0 || B < 2 || C < 1 || C > (int64_t(1) << 30) || rows != N * (B - 1)) return XP_ERR_SHAPE;
+  if (rows == 0) return XP_OK;
+  if (!d_base_c || !d_bias_c || !d_cand || !d_blk) return XP_ERR_NULL;
+  if (((uintptr_t)d_base_c & 1) || ((uintptr_t)d_bias_c & 1) || ((uintptr_t)d_cand & 7) || ((uintptr_t)d_blk & 7))
+    return XP_ERR_ALIGN;
+  xp_status st = check_device();
+  if (st != XP_OK) return st;
+  return xp::launch_topc_argmax(d_base_c, d_bias_c, d_cand, rows, C, d_blk, B, (cudaStream_t)stream);
+}
+
 size_t xp_latent_workspace_size(int64_t N, int64_t B, int64_t D, int64_t R, int64_t H) {
   if (N < 0 || B < 2 || D < 0 || R < 0 || H < 0) return 0;
   return xp::latent_ws_layout(N, B, D, R, H).total_latent;
@@ -176,6 +188,43 @@ xp_status xp_jacobi_pass(int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_
   if (st != XP_OK) return st;
   return xp::launch_readout_argmax(lat, d_W2t, d_base, ld_base, N * (B - 1), V, R, d_blk, B, d_changed, d_workspace,
                                    (cudaStream_t)stream);
+}
+
+xp_status xp_jacobi_fixpoint(int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_hcache, const xp_bf16* d_E,
+                             const xp_bf16* d_W_lat, const float* d_L, const xp_bf16* d_Wg, const xp_bf16* d_Wu,
+                             const xp_bf16* d_Wd, const xp_bf16* d_W2t, const xp_bf16* d_base, int64_t ld_base,
+                             int64_t N, int64_t B, int64_t V, int64_t D, int64_t R, int64_t H, int32_t max_passes,
+                             int32_t* d_passes, int32_t* d_changed, void* d_workspace, size_t workspace_bytes,
+                             xp_stream_t stream) {
+  xp_status st = check_latent_args(d_blk, d_am1, d_hcache, d_E, d_W_lat, d_L, d_Wg, d_Wu, d_Wd, N, B, V, D, R, H);
+  if (st != XP_OK) return st;
+  if (ld_base < V || max_passes < 1 || max_passes > 1024) return XP_ERR_SHAPE;
+  if (!d_W2t || !d_base || !d_workspace || !d_passes) return XP_ERR_NULL;
+  if (!aligned16(d_W2t) || !aligned16(d_base) || (ld_base & 7) || ((uintptr_t)d_changed & 3) ||
+      ((uintptr_t)d_passes & 3))
+    return XP_ERR_ALIGN;
+  const xp::LatentWsLayout lay = xp::latent_ws_layout(N, B, D, R, H);
+  if (!aligned256(d_workspace) || workspace_bytes < lay.total_pass) return XP_ERR_WORKSPACE;
+  st = check_device();
+  if (st != XP_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  xp::WsHeader* hdr = static_cast<xp::WsHeader*>(d_workspace);
+  // converged = 0, passes = 0 (adjacent fields); then N == 0 runs no pass
+  if (cudaMemsetAsync(&hdr->converged, 0, 2 * sizeof(unsigned int), s) != cudaSuccess ||
+      cudaMemsetAsync(d_passes, 0, sizeof(int32_t), s) != cudaSuccess)
+    return XP_ERR_LAUNCH;
+  if (N == 0) return XP_OK;
+  uint16_t* lat = reinterpret_cast<uint16_t*>(static_cast<char*>(d_workspace) + lay.lat);
+  const uint32_t* skip = &hdr->converged;
+  for (int32_t k = 0; k < max_passes; ++k) {
+    st = xp::launch_latent(d_blk, d_am1, d_hcache, d_E, d_W_lat, d_L, d_Wg, d_Wu, d_Wd, lat, N, B, V, D, R, H,
+                           d_workspace, s, skip);
+    if (st != XP_OK) return st;
+    st = xp::launch_readout_argmax(lat, d_W2t, d_base, ld_base, N * (B - 1), V, R, d_blk, B, d_changed, d_workspace,
+                                   s, skip, d_passes);
+    if (st != XP_OK) return st;
+  }
+  return XP_OK;
 }
 
 xp_status xp_read_error(void* d_workspace, xp_stream_t stream, uint32_t* host_bits) {

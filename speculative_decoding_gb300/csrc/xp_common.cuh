@@ -81,7 +81,11 @@ struct WsHeader {
   unsigned int err;         // XP_DEVERR_* bits
   unsigned int done;        // CTAs of the current readout grid that finished
   unsigned int where;       // site code of the first wait that gave up (diagnostics)
-  unsigned int pad[61];
+  // xp_jacobi_fixpoint: nonzero once a pass changed no slot (the passes
+  // launched after it exit at once), and the number of passes that ran
+  unsigned int converged;
+  unsigned int passes;
+  unsigned int pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

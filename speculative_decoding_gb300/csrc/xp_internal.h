@@ -16,13 +16,21 @@ xp_status launch_add_argmax(const uint16_t* base, int64_t ld_base, const uint16_
 xp_status launch_add_argmax_noalloc(const uint16_t* base, int64_t ld_base, const uint16_t* bias, int64_t ld_bias,
                                     int64_t rows, int64_t V, int64_t* blk, int64_t B, cudaStream_t stream);
 
+// xp_topc_argmax: one warp per row, no workspace.
+xp_status launch_topc_argmax(const uint16_t* base_c, const uint16_t* bias_c, const int64_t* cand, int64_t rows,
+                             int64_t C, int64_t* blk, int64_t B, cudaStream_t stream);
+
+// skip (nullable): the pass's fixpoint flag (pass_skipped); passes_out
+// (nullable, with skip): the readout's last CTA counts the pass there and
+// sets the flag when the pass changed no slot.
 xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const uint16_t* base, int64_t ld_base,
                                 int64_t rows, int64_t V, int64_t R, int64_t* blk, int64_t B, int32_t* changed,
-                                void* ws, cudaStream_t stream);
+                                void* ws, cudaStream_t stream, const uint32_t* skip = nullptr,
+                                int32_t* passes_out = nullptr);
 
 xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* hcache, const uint16_t* E,
                         const uint16_t* W_lat, const float* L, const uint16_t* Wg, const uint16_t* Wu,
                         const uint16_t* Wd, uint16_t* lat_out, int64_t N, int64_t B, int64_t V, int64_t D, int64_t R,
-                        int64_t H, void* ws, cudaStream_t stream);
+                        int64_t H, void* ws, cudaStream_t stream, const uint32_t* skip = nullptr);
 
 }  // namespace xp

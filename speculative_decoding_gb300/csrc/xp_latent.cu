@@ -76,6 +76,7 @@ struct ProjParams {
   int32_t N, B, V, D, R, bpt, tn, S, w, chunks, ntiles, stages;
   int64_t rows_pad, r_pad;
   uint32_t region, hc_off, tok_off, bar_off;
+  const uint32_t* skip;  // nullable: see pass_skipped
 };
 
 __host__ __device__ inline uint32_t proj_ls_bytes(int B, int w) {
@@ -87,6 +88,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
                 const __grid_constant__ CUtensorMap mapPart, const __grid_constant__ CUtensorMap mapPartSt,
                 const ProjParams p) {
   extern __shared__ uint8_t smem_raw[];
+  if (pass_skipped(p.skip)) return;
   if (threadIdx.x == 0) XP_TRACE_MARK(0);
   if (threadIdx.x == 0) XP_TRACE_SM(15);
   uint8_t* smem = align1024(smem_raw);
@@ -419,12 +421,14 @@ struct UpParams {
   uint16_t* m;
   WsHeader* hdr;
   int32_t rows, H, chunks, htiles, stages;
+  const uint32_t* skip;  // nullable: see pass_skipped
 };
 
 __global__ void __launch_bounds__(LT_THREADS, 1)
 mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__ CUtensorMap mapWg,
               const __grid_constant__ CUtensorMap mapWu, const UpParams p) {
   extern __shared__ uint8_t smem_raw[];
+  if (pass_skipped(p.skip)) return;
   if (threadIdx.x == 0) XP_TRACE_MARK(16);
   uint8_t* smem = align1024(smem_raw);
   constexpr uint32_t stage_bytes = LT_A_CHUNK + 2 * LT_BOX;  // 32 KB
@@ -573,12 +577,14 @@ struct DownParams {
   WsHeader* hdr;
   int32_t N, B, R, tn, S, w, chunks, ntiles, stages;
   uint32_t region, bar_off;
+  const uint32_t* skip;  // nullable: see pass_skipped
 };
 
 __global__ void __launch_bounds__(LT_THREADS, 2)
 mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant__ CUtensorMap mapWd,
                 const __grid_constant__ CUtensorMap mapU, const DownParams p) {
   extern __shared__ uint8_t smem_raw[];
+  if (pass_skipped(p.skip)) return;
   if (threadIdx.x == 0) XP_TRACE_MARK(32);
   uint8_t* smem = align1024(smem_raw);
   const uint32_t b_bytes = (uint32_t)p.tn * LT_BK * 2;
@@ -809,7 +815,7 @@ int pow2_floor(int x, int cap) {
 xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* hcache, const uint16_t* E,
                         const uint16_t* W_lat, const float* L, const uint16_t* Wg, const uint16_t* Wu,
                         const uint16_t* Wd, uint16_t* lat_out, int64_t N, int64_t B, int64_t V, int64_t D, int64_t R,
-                        int64_t H, void* ws, cudaStream_t stream) {
+                        int64_t H, void* ws, cudaStream_t stream, const uint32_t* skip) {
   if (N <= 0) return XP_OK;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return XP_ERR_LAUNCH;
@@ -817,14 +823,17 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     int max_smem = 0;
     if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
       return XP_ERR_LAUNCH;
-    // the largest shared-memory carve-out, so two ~110 KB CTAs fit an SM
-    if (cudaFuncSetAttribute(proj_mix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(mlp_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) != cudaSuccess ||
-        cudaFuncSetAttribute(mlp_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(proj_mix_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess ||
-        cudaFuncSetAttribute(mlp_down_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+    // the largest dynamic shared memory each kernel may ask for (the opt-in
+    // maximum less its static shared memory) and the largest carve-out
+    auto allow = [&](const void* fn) {
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return false;
+      return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  max_smem - (int)fa.sharedSizeBytes) == cudaSuccess &&
+             cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
+    };
+    if (!allow((const void*)proj_mix_kernel) || !allow((const void*)mlp_up_kernel) ||
+        !allow((const void*)mlp_down_kernel))
       return XP_ERR_LAUNCH;
     g_lt_attr[dev] = true;
   }
@@ -840,6 +849,7 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
   {
     const ProjTiling t = proj_tiling(N, B, D, R);
     ProjParams p;
+    p.skip = skip;
     p.blk = blk;
     p.am1 = am1;
     p.E = E;
@@ -896,6 +906,7 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
   // ---- mlp_up
   {
     UpParams p;
+    p.skip = skip;
     p.m = m;
     p.hdr = hdr;
     p.rows = rows;
@@ -918,6 +929,7 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
   // ---- mlp_down
   {
     DownParams p;
+    p.skip = skip;
     p.lat = lat_out;
     p.hdr = hdr;
     p.N = (int32_t)N;

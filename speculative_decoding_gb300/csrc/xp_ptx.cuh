@@ -364,6 +364,22 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
 // programmatic dependent launch: wait for the preceding kernel's results /
 // let the next kernel start its prologue
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Multi-pass launches of a fixed count: every kernel of a pass launched after
+// the fixpoint was reached exits at once.  `skip` (nullable) is the flag the
+// last pass's readout set; thread 0 reads it after the dependency wait (the
+// preceding kernels, and through them the pass that set it, are complete),
+// and the CTA agrees on it.  Returns true when this CTA must exit.
+__device__ __forceinline__ bool pass_skipped(const uint32_t* skip) {
+  __shared__ uint32_t s_skip;
+  if (skip == nullptr) return false;
+  if (threadIdx.x == 0) {
+    pdl_wait();
+    s_skip = *reinterpret_cast<const volatile uint32_t*>(skip);
+  }
+  __syncthreads();
+  return s_skip != 0u;
+}
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

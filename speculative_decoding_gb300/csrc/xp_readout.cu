@@ -79,6 +79,8 @@ struct ReadoutParams {
   int32_t* changed;
   unsigned long long* keys;
   WsHeader* hdr;
+  const uint32_t* skip;  // nullable: see pass_skipped
+  int32_t* passes_out;   // nullable: fixpoint pass count (with skip)
 };
 
 // One 32-column chunk of one row: acc (fp32) -> bias = bf16(acc);
@@ -131,6 +133,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   uint64_t* a_free = a_full + 2;  // the epilogue warps copied a round to TMEM
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(a_free + 1);
   __shared__ int s_last;
+  if (pass_skipped(p.skip)) return;  // both CTAs of a pair read the same flag
   if (threadIdx.x == 0) XP_TRACE_MARK(0);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -457,7 +460,15 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       *slot = idx;
     }
     if (p.changed && nchanged) atomicAdd(p.changed, nchanged);
-    __syncthreads();
+    // fixpoint driver: count the pass; a pass that changed no slot is the
+    // last one (the passes launched after it exit at once)
+    const int any_changed = __syncthreads_or(nchanged);
+    if (p.passes_out && threadIdx.x == 0) {
+      const uint32_t np = p.hdr->passes + 1u;
+      p.hdr->passes = np;
+      *p.passes_out = (int32_t)np;
+      if (!any_changed) p.hdr->converged = 1u;
+    }
     if (threadIdx.x == 0) p.hdr->done = 0u;
   }
   if (threadIdx.x == 0) XP_TRACE_MARK(6);
@@ -494,7 +505,7 @@ RoDevInfo g_ro_dev[64];
 
 xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const uint16_t* base, int64_t ld_base,
                                 int64_t rows, int64_t V, int64_t R, int64_t* blk, int64_t B, int32_t* changed,
-                                void* ws, cudaStream_t stream) {
+                                void* ws, cudaStream_t stream, const uint32_t* skip, int32_t* passes_out) {
   if (rows <= 0) return XP_OK;
   const int kch = (int)((R + 63) / 64);
   if (kch > RO_MAX_KCH) return XP_ERR_SHAPE;
@@ -538,6 +549,8 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
   p.changed = changed;
   p.keys = w.keys;
   p.hdr = w.hdr;
+  p.skip = skip;
+  p.passes_out = passes_out;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -40,6 +40,7 @@ _SIGS = {
     "xp_add_argmax_workspace_size": (_sz, [_i64, _i64]),
     "xp_add_argmax": (ctypes.c_int32, [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _sz, _vp]),
     "xp_add_argmax_noalloc": (ctypes.c_int32, [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp]),
+    "xp_topc_argmax": (ctypes.c_int32, [_vp, _vp, _vp, _i64, _i64, _vp, _i64, _i64, _vp]),
     "xp_latent_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _i64]),
     "xp_latent_pass": (ctypes.c_int32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                         _i64, _i64, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
@@ -49,6 +50,9 @@ _SIGS = {
     "xp_jacobi_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _i64, _i64]),
     "xp_jacobi_pass": (ctypes.c_int32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
                                         _i64, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
+    "xp_jacobi_fixpoint": (ctypes.c_int32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
+                                            _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int32, _vp, _vp, _vp,
+                                            _sz, _vp]),
     "xp_read_error": (ctypes.c_int32, [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]),
 }
 
@@ -137,6 +141,17 @@ def add_argmax_noalloc(base, bias, blk, stream=None) -> None:
                                        rows, V, _ptr(blk, torch.int64, "blk"), N, B, _stream(stream)))
 
 
+def topc_argmax(base_c, bias_c, cand, blk, stream=None) -> None:
+    """blk[n, 1+j] = cand[r, p*], p* the lowest argmax_p bf16(base_c[r, p] + bias_c[r, p]);
+    base_c, bias_c, cand are [N, B-1, C] (or [rows, C])."""
+    C = base_c.shape[-1]
+    rows = base_c.numel() // C if C else 0
+    N, B = blk.shape
+    _check(lib().xp_topc_argmax(_ptr(base_c, torch.bfloat16, "base_c"), _ptr(bias_c, torch.bfloat16, "bias_c"),
+                                _ptr(cand, torch.int64, "cand"), rows, C, _ptr(blk, torch.int64, "blk"), N, B,
+                                _stream(stream)))
+
+
 def latent_workspace_size(N: int, B: int, D: int, R: int, H: int) -> int:
     return int(lib().xp_latent_workspace_size(N, B, D, R, H))
 
@@ -188,6 +203,24 @@ def jacobi_pass(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, W2t, base, ws, change
                                 _rowmajor(base, "base"), N, B, V, D, R, H,
                                 _ptr(changed, torch.int32, "changed"),
                                 _ptr(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream)))
+
+
+def jacobi_fixpoint(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, W2t, base, ws, passes, max_passes=8,
+                    changed=None, stream=None) -> None:
+    """Passes in place on blk until one changes nothing (counted) or max_passes;
+    the count lands in the device int32 tensor ``passes`` (no host sync)."""
+    N, B = blk.shape
+    V, D = E.shape
+    R = W_lat.shape[1]
+    H = Wg.shape[1]
+    bf = torch.bfloat16
+    _check(lib().xp_jacobi_fixpoint(_ptr(blk, torch.int64, "blk"), _ptr(am1, torch.int64, "am1"),
+                                    _ptr(hcache, bf, "hcache"), _ptr(E, bf, "E"), _ptr(W_lat, bf, "W_lat"),
+                                    _ptr(L, torch.float32, "L"), _ptr(Wg, bf, "Wg"), _ptr(Wu, bf, "Wu"),
+                                    _ptr(Wd, bf, "Wd"), _ptr(W2t, bf, "W2t"), _ptr(base, bf, "base", False),
+                                    _rowmajor(base, "base"), N, B, V, D, R, H, int(max_passes),
+                                    _ptr(passes, torch.int32, "passes"), _ptr(changed, torch.int32, "changed"),
+                                    _ptr(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream)))
 
 
 def read_error(ws, stream=None) -> int:

@@ -130,3 +130,62 @@ def test_full_size_pass_sampled(orc):
     rows = sorted(set(list(range(0, shape.rows, 15)) + rng.choice(shape.rows, 16, replace=False).tolist()))
     exact = check_rows(orc, d, d["blk"], out, rows)
     assert exact >= len(rows) - 2
+
+
+def _fixpoint_run(p, blk_np, max_passes):
+    blk = dev(blk_np.copy())
+    passes = torch.zeros(1, dtype=torch.int32, device="cuda")
+    changed = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t = p.t
+    xpress.jacobi_fixpoint(blk, p.am1, t["hcache"], t["E"], t["W_lat"], p.L, t["Wg"], t["Wu"], t["Wd"], t["W2t"],
+                           t["base"], p.ws, passes, max_passes=max_passes, changed=changed)
+    torch.cuda.synchronize()
+    assert xpress.read_error(p.ws) == 0
+    return blk.cpu().numpy(), int(passes.item()), int(changed.item())
+
+
+@pytest.mark.parametrize("cap", [3, 16])
+def test_fixpoint_driver_matches_pass_loop(cap):
+    """xp_jacobi_fixpoint (all passes enqueued, no host round trip) against the
+    host loop of xp_jacobi_pass that stops after the first pass that changed
+    nothing: same final blk, same pass count (the kernels are deterministic),
+    and the passes after the fixpoint leave blk alone."""
+    shape = synth.PassShape("fp", 6, 8, 2000, 128, 64, 128, 41)
+    d = synth.pass_inputs(shape)
+    d["base"] = synth.to_bf16_bits(_f(d["base"]) * np.float32(0.05))
+    d["W2"] = synth.to_bf16_bits(_f(d["W2"]) * np.float32(8.0))
+    p = Pass(d, shape)
+    blk, n, total = d["blk"].copy(), 0, 0
+    while n < cap:
+        blk, changed = p.run(blk)
+        n += 1
+        total += changed
+        if changed == 0:
+            break
+    got, passes, changed = _fixpoint_run(p, d["blk"], cap)
+    np.testing.assert_array_equal(got, blk)
+    assert passes == n and changed == total
+    if cap == 16:
+        assert n < cap  # this input converges within B passes
+
+
+def test_fixpoint_full_size_eight_passes(orc):
+    """The multi-pass workload: N=64, B=16, V=152064, D=3584, R=512, H=1536,
+    at most 8 passes.  Same blk and count as the host pass loop; the count
+    equals the oracle's when its trajectory is the GPU's (teacher-forced
+    check of the last pass on sampled rows)."""
+    shape = synth.FIXPOINT
+    d = synth.pass_inputs(shape)
+    p = Pass(d, shape)
+    blk, n, prev = d["blk"].copy(), 0, None
+    while n < 8:
+        prev = blk
+        blk, changed = p.run(blk)
+        n += 1
+        if changed == 0:
+            break
+    got, passes, _ = _fixpoint_run(p, d["blk"], 8)
+    np.testing.assert_array_equal(got, blk)
+    assert passes == n
+    rows = list(range(0, shape.rows, 37))
+    check_rows(orc, d, prev, blk, rows)
