@@ -325,6 +325,52 @@ def run_gb300(args, rank, world, local_rank):
         aa_us = events_time(stream, am, args.steps) / args.steps
         aa_bytes = synth.ARGMAX_ROWS * synth.ARGMAX_V * 4
 
+        # ---- latency floor: one block (N=1, B=16, same model dims), the pass
+        # captured once in a CUDA graph and replayed (inputs stay resident)
+        fa = synth.pass_activations(synth.FLOOR)
+        f_in = dict(hcache=dev_bf16(fa["hcache"], device), base=dev_bf16(fa["base"], device),
+                    am1=torch.from_numpy(fa["am1"]).to(device), blk=torch.from_numpy(fa["blk"]).to(device))
+        fws = xpress.workspace(xpress.jacobi_workspace_size(1, B, V, D, R, H), device)
+
+        def floor_pass():
+            xpress.jacobi_pass(f_in["blk"], f_in["am1"], f_in["hcache"], w["E"], w["W_lat"], L, w["Wg"], w["Wu"],
+                               w["Wd"], w["W2t"], f_in["base"], fws)
+
+        for _ in range(3):
+            floor_pass()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            floor_pass()
+        graph.replay()
+        torch.cuda.synchronize()
+        floor_reps = 10000
+        floor_us = events_time(stream, lambda i: graph.replay(), floor_reps) / floor_reps
+        if xpress.read_error(fws) != 0:
+            raise RuntimeError("device-side error bits set in the latency-floor replays")
+
+        # ---- multi-pass: N=64, B=16, passes to the fixpoint (at most 8), all
+        # enqueued at once (xp_jacobi_fixpoint), no host round trip
+        xa = synth.pass_activations(synth.FIXPOINT)
+        x_in = dict(hcache=dev_bf16(xa["hcache"], device), base=dev_bf16(xa["base"], device),
+                    am1=torch.from_numpy(xa["am1"]).to(device), blk0=torch.from_numpy(xa["blk"]).to(device))
+        x_blk = x_in["blk0"].clone()
+        xws = xpress.workspace(xpress.jacobi_workspace_size(synth.FIXPOINT.N, B, V, D, R, H), device)
+        x_passes = torch.zeros(1, dtype=torch.int32, device=device)
+
+        def fixpoint(i):
+            x_blk.copy_(x_in["blk0"])
+            xpress.jacobi_fixpoint(x_blk, x_in["am1"], x_in["hcache"], w["E"], w["W_lat"], L, w["Wg"], w["Wu"],
+                                   w["Wd"], w["W2t"], x_in["base"], xws, x_passes, max_passes=8)
+
+        fixpoint(0)
+        torch.cuda.synchronize()
+        fx_reps = max(3, min(20, args.steps))
+        fx_us = events_time(stream, fixpoint, fx_reps) / fx_reps
+        fx_passes = int(x_passes.item())
+        if xpress.read_error(xws) != 0:
+            raise RuntimeError("device-side error bits set in the multi-pass runs")
+
         # ---- end to end through the binding, host buffers, copies inside
         host = [dict(hcache=torch.from_numpy(src["hcache"].view(np.int16)).view(torch.bfloat16).pin_memory(),
                      base=torch.from_numpy(src["base"].view(np.int16)).view(torch.bfloat16).pin_memory(),
@@ -383,6 +429,11 @@ def run_gb300(args, rank, world, local_rank):
                  "roofline_us": round(max(pass_bytes(sh) / hbm_peak / 1e3, pass_flops(sh) / tf_peak / 1e6), 2),
                  "frac_of_roofline": round(max(pass_bytes(sh) / hbm_peak / 1e3,
                                                pass_flops(sh) / tf_peak / 1e6) / per_pass, 3)},
+        "latency_floor": {"workload": "pass N=1 B=16 V=152064 D=3584 R=512 H=1536, CUDA graph replay",
+                          "replays": floor_reps, "us_per_pass": round(floor_us, 2)},
+        "multipass": {"workload": "fixpoint N=64 B=16 V=152064 D=3584 R=512 H=1536, at most 8 passes",
+                      "passes": fx_passes, "us_per_call": round(fx_us, 2),
+                      "us_per_pass": round(fx_us / max(1, fx_passes), 2)},
         "add_argmax": {"workload": "rows=480 V=152064 base+bias bf16", "us": round(aa_us, 2),
                        "GBps": round(aa_bytes / aa_us / 1e3, 1),
                        "frac": round(aa_bytes / aa_us / 1e3 / hbm_peak, 3), "peak": f"{peak_kind} {hbm_peak} GB/s",

@@ -143,6 +143,16 @@ def pass_inputs(shape: PassShape, with_embedding: bool = True) -> dict:
     return out
 
 
+def pass_activations(shape: PassShape) -> dict:
+    """The per-pass inputs of ``pass_inputs`` (hcache, base, am1, blk: the same
+    values, same streams) without the weights, for runs that reuse the weights
+    of another workload of the same model dimensions."""
+    s, N, B, V, R = shape.seed, shape.N, shape.B, shape.V, shape.R
+    return dict(hcache=normal_bf16(s, _S["hcache"], (N, B, R), 1.0),
+                base=normal_bf16(s, _S["base"], (N * (B - 1), V), 3.0),
+                am1=tokens(s, _S["am1"], (N,), V), blk=tokens(s, _S["blk"], (N, B), V))
+
+
 def plant_ties(base: np.ndarray, bias: np.ndarray, frac: float, seed: int, min_rows: int = 1):
     """Plant duplicated row maxima, in place.
 
