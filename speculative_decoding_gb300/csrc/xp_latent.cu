@@ -53,8 +53,10 @@ __device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float((uint
 // ============================================================================
 // Shared memory: [0, region) is the stage ring; once the MMAs are done it holds
 // the S partial-sum slices of this CTA's w columns (TMA from the partial
-// buffer) and xs[128][w] (the reduced x).  After it: Ls (the mixer weights of
-// those columns, lower triangle packed by rows), hcs (the hidden cache of
+// buffer) and xs[128][w] (the reduced x), then the outgoing partial tile and,
+// once that is stored, the mixer output tiles us [rows][w] fp32 and ubs
+// [rows][w] bf16 (TMA-stored).  After it: Ls (the mixer weights of those
+// columns, the [B][B] square), hcs (the hidden cache of
 // those columns for the tile's 128 rows), the token table and the barriers.
 //
 // The S CTAs of a tile (one per slice of the D-long reduction) are ordinary
@@ -79,14 +81,15 @@ struct ProjParams {
   const uint32_t* skip;  // nullable: see pass_skipped
 };
 
-__host__ __device__ inline uint32_t proj_ls_bytes(int B, int w) {
-  return (uint32_t)(((B * (B + 1) / 2) * w * 4 + 127) & ~127);
-}
+// the mixer weights of a CTA's w columns: the full [B][B] square (one TMA
+// box; entries above the diagonal are loaded and ignored)
+__host__ __device__ inline uint32_t proj_ls_bytes(int B, int w) { return (uint32_t)((B * B * w * 4 + 127) & ~127); }
 
 __global__ void __launch_bounds__(LT_THREADS, 1)
 proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_constant__ CUtensorMap mapHc,
                 const __grid_constant__ CUtensorMap mapPart, const __grid_constant__ CUtensorMap mapPartSt,
-                const ProjParams p) {
+                const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUtensorMap mapU,
+                const __grid_constant__ CUtensorMap mapUb, const ProjParams p) {
   extern __shared__ uint8_t smem_raw[];
   if (pass_skipped(p.skip)) return;
   if (threadIdx.x == 0) XP_TRACE_MARK(0);
@@ -153,30 +156,25 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     // the MMAs) go after the first W_lat stages.  Lane 0 waits for a stage and
     // arms its barrier; lanes 0..tn/64-1 issue one W_lat box each (a single
     // thread issues tiled copies slowly).
-    const int tri = p.B * (p.B + 1) / 2;
+    // two boxes: the hidden-cache slice and the mixer weights of the slice
+    // (the whole [B][B] square of L for these w channels)
     auto aux_copies = [&]() {
       if (lane == 0) {
-        mbar_arrive_expect_tx(aux_full, (uint32_t)(tri * wv * 4) + (uint32_t)(LT_BM * p.w * 2));
+        mbar_arrive_expect_tx(aux_full, (uint32_t)(p.B * p.B * p.w * 4) + (uint32_t)(LT_BM * p.w * 2));
         tma_load_2d(smem + p.hc_off, &mapHc, col0, mt * p.bpt * p.B, aux_full);
+        tma_load_2d(Ls, &mapL, col0, 0, aux_full);
       }
       __syncwarp();
-      if (wv > 0) {
-        for (int pr = lane; pr < tri; pr += 32) {
-          int b = 0;
-          while ((b + 1) * (b + 2) / 2 <= pr) ++b;
-          const int j = pr - b * (b + 1) / 2;
-          bulk_load(Ls + pr * p.w, p.L + ((int64_t)b * p.B + j) * p.R + col0, (uint32_t)wv * 4, aux_full);
-        }
-      }
     };
     const uint64_t pol = policy_evict_last();  // every pass re-reads W_lat
     if (lane == 0) {
       prefetch_tensormap(&mapWlat);
       prefetch_tensormap(&mapHc);
       prefetch_tensormap(&mapPart);
+      prefetch_tensormap(&mapL);
     }
     for (int i = 0; i < nck; ++i) {
-      if (i == p.stages) aux_copies();
+      if (i == 1) aux_copies();
       const uint32_t s = i % p.stages, k = i / p.stages;
       int ok = 1;
       if (lane == 0) {
@@ -192,7 +190,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
         tma_load_2d_hint(smem + (size_t)s * stage_bytes + LT_A_CHUNK + lane * LT_BOX, &mapWlat,
                          nt * p.tn + lane * 64, (c0 + i) * LT_BK, &full[s], pol);
     }
-    if (nck <= p.stages) aux_copies();
+    if (nck <= 1) aux_copies();
     if (lane == 0) XP_TRACE_MARK(3);
   } else if (warp == 1) {
     if (lane == 0) {
@@ -381,12 +379,13 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     }
     if (et == 127) XP_TRACE_MARK(12);
     named_barrier_sync(1, 128);
-    // ---- the causal mixer on this CTA's columns: u[b] = sum_{j<=b} L[b,j] x[j]
+    // ---- the causal mixer on this CTA's columns: u[b] = sum_{j<=b} L[b,j] x[j],
+    // into shared-memory tiles of the tile's rows (rows past N*B and columns
+    // past R are clipped by the stores)
+    float* us = reinterpret_cast<float*>(pst);                            // [bpt*B][w]
+    uint16_t* ubs = reinterpret_cast<uint16_t*>(pst + (size_t)LT_BM * p.w * 4);  // [bpt*B][w]
     for (int it = et; it < nbl * p.w; it += 128) {
       const int bl = it / p.w, c = it - bl * p.w;
-      const int col = col0 + c;
-      if (c >= wv) continue;
-      const int n = mt * p.bpt + bl;
       float x[LT_MAX_B];
 #pragma unroll
       for (int j = 0; j < LT_MAX_B; ++j) x[j] = j < p.B ? xs[(bl * p.B + j) * p.w + c] : 0.f;
@@ -394,16 +393,24 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
       for (int b = 0; b < LT_MAX_B; ++b) {
         if (b < p.B) {
           float uu = 0.f;
-          const float* Lb = Ls + (b * (b + 1) / 2) * p.w + c;
+          const float* Lb = Ls + (b * p.B) * p.w + c;
 #pragma unroll
           for (int j = 0; j <= b; ++j) uu = fmaf(Lb[j * p.w], x[j], uu);
-          const int64_t o = ((int64_t)n * p.B + b) * p.R + col;
-          p.u[o] = uu;
-          p.ub[o] = (uint16_t)(f32x2_to_bf16x2(uu, 0.f) & 0xffffu);
+          const int o = (bl * p.B + b) * p.w + c;
+          us[o] = uu;
+          ubs[o] = (uint16_t)(f32x2_to_bf16x2(uu, 0.f) & 0xffffu);
         }
       }
     }
-    if (et == 0) XP_TRACE_MARK(13);
+    fence_proxy_async_smem();
+    named_barrier_sync(1, 128);
+    if (et == 0) {
+      tma_store_2d(&mapU, us, col0, mt * p.bpt * p.B);
+      tma_store_2d(&mapUb, ubs, col0, mt * p.bpt * p.B);
+      bulk_commit();
+      bulk_wait_all();
+      XP_TRACE_MARK(13);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -890,15 +897,21 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     // Ls, hcs, the token table, then full/empty per stage, acc_full,
     // aux_full, slice_full and the TMEM address slot
     const size_t smem = 1024 + (size_t)p.bar_off + 8 * (2 * p.stages + 3) + 16;
-    CUtensorMap mapWlat, mapHc, mapPart, mapPartSt;
+    CUtensorMap mapWlat, mapHc, mapPart, mapPartSt, mapL, mapU, mapUbS;
     if (!cached_map_bf16_2d(&mapWlat, W_lat, (uint64_t)R, (uint64_t)D, (uint64_t)R, 64, LT_BK) ||
         !cached_map_plain_2d(&mapHc, hcache, 2, (uint64_t)R, (uint64_t)(N * B), (uint64_t)R, (uint32_t)t.w, LT_BM) ||
         !cached_map_plain_2d(&mapPart, p.part, 4, (uint64_t)t.r_pad, (uint64_t)(t.S * t.rows_pad), (uint64_t)t.r_pad,
                              (uint32_t)t.w, LT_BM) ||
         !cached_map_plain_2d(&mapPartSt, p.part, 4, (uint64_t)t.r_pad, (uint64_t)(t.S * t.rows_pad),
-                             (uint64_t)t.r_pad, 32, LT_BM, true))
+                             (uint64_t)t.r_pad, 32, LT_BM, true) ||
+        !cached_map_plain_2d(&mapL, L, 4, (uint64_t)R, (uint64_t)(B * B), (uint64_t)R, (uint32_t)t.w,
+                             (uint32_t)(B * B)) ||
+        !cached_map_plain_2d(&mapU, u, 4, (uint64_t)R, (uint64_t)(N * B), (uint64_t)R, (uint32_t)t.w,
+                             (uint32_t)(t.bpt * B)) ||
+        !cached_map_plain_2d(&mapUbS, ub, 2, (uint64_t)R, (uint64_t)(N * B), (uint64_t)R, (uint32_t)t.w,
+                             (uint32_t)(t.bpt * B)))
       return XP_ERR_LAUNCH;
-    void* args[] = {&mapWlat, &mapHc, &mapPart, &mapPartSt, &p};
+    void* args[] = {&mapWlat, &mapHc, &mapPart, &mapPartSt, &mapL, &mapU, &mapUbS, &p};
     if (launch_ex((const void*)proj_mix_kernel, dim3((unsigned)(t.mtiles * t.ntiles * t.S)), smem, stream, 1, args) !=
         cudaSuccess)
       return XP_ERR_LAUNCH;

@@ -72,7 +72,7 @@ inline bool cached_map_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner
     bool nan;
     CUtensorMap map;
   };
-  static thread_local Entry cache[16];
+  static thread_local Entry cache[32];
   static thread_local unsigned next = 0;
   for (auto& e : cache)
     if (e.ptr == ptr && e.inner == inner && e.outer == outer && e.ld == ld && e.bi == box_inner &&
@@ -81,7 +81,7 @@ inline bool cached_map_bf16_2d(CUtensorMap* map, const void* ptr, uint64_t inner
       return true;
     }
   if (!make_map_bf16_2d(map, ptr, inner, outer, ld, box_inner, box_outer, nan_fill)) return false;
-  Entry& e = cache[next++ % 16];
+  Entry& e = cache[next++ % 32];
   e.ptr = ptr;
   e.nan = nan_fill;
   e.inner = inner;
@@ -104,7 +104,7 @@ inline bool cached_map_plain_2d(CUtensorMap* map, const void* ptr, uint32_t elem
     bool sw;
     CUtensorMap map;
   };
-  static thread_local Entry cache[8];
+  static thread_local Entry cache[32];
   static thread_local unsigned next = 0;
   for (auto& e : cache)
     if (e.ptr == ptr && e.eb == elem_bytes && e.inner == inner && e.outer == outer && e.ld == ld &&
@@ -113,7 +113,7 @@ inline bool cached_map_plain_2d(CUtensorMap* map, const void* ptr, uint32_t elem
       return true;
     }
   if (!make_map_plain_2d(map, ptr, elem_bytes, inner, outer, ld, box_inner, box_outer, swizzle128)) return false;
-  Entry& e = cache[next++ % 8];
+  Entry& e = cache[next++ % 32];
   e.ptr = ptr;
   e.sw = swizzle128;
   e.eb = elem_bytes;
