@@ -125,8 +125,13 @@ __host__ inline ProjTiling proj_tiling(int64_t N, int64_t B, int64_t D, int64_t 
   t.tn = R >= 128 ? 128 : 64;
   t.ntiles = (int32_t)((R + t.tn - 1) / t.tn);
   t.chunks = (int32_t)((D + 63) / 64);
+  // as many slices as keep the grid within 128 CTAs (one wave at one CTA
+  // per SM, so the S CTAs of a tile that wait for each other are resident
+  // together), at most 16 and at least 8 channels per CTA
   t.S = 1;
-  while (t.S * 2 <= t.chunks && t.S * 2 <= 8) t.S *= 2;
+  while (t.S * 2 <= t.chunks && t.S * 2 <= 16 && t.tn / (t.S * 2) >= 8 &&
+         (int64_t)t.mtiles * t.ntiles * t.S * 2 <= 128)
+    t.S *= 2;
   t.w = t.tn / t.S;
   t.rows_pad = (int64_t)t.mtiles * 128;
   t.r_pad = (int64_t)t.ntiles * t.tn;

@@ -817,6 +817,10 @@ int pow2_floor(int x, int cap) {
   return s;
 }
 
+// Dynamic shared memory a kernel here may use: the 227 KB opt-in maximum less
+// the static shared memory and a margin.
+constexpr size_t kSmemBudget = 226 * 1024;
+
 }  // namespace
 
 xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* hcache, const uint16_t* E,
@@ -888,15 +892,21 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     const size_t hc = ((size_t)LT_BM * t.w * 2 + 127) & ~size_t(127);
     // the gathering warps keep stages - 1 stages in flight
     const int per_cta = (t.chunks + t.S - 1) / t.S;
-    p.stages = per_cta < 6 ? (per_cta < 2 ? 2 : per_cta) : 6;
-    const size_t ring = (size_t)p.stages * stage_bytes;
-    p.region = (uint32_t)((ring > sl_xs ? ring : sl_xs + 1023) & ~size_t(1023));
-    p.hc_off = p.region + (uint32_t)ls;
-    p.tok_off = p.hc_off + (uint32_t)hc;
-    p.bar_off = p.tok_off + 8 * LT_BM;
     // Ls, hcs, the token table, then full/empty per stage, acc_full,
-    // aux_full, slice_full and the TMEM address slot
-    const size_t smem = 1024 + (size_t)p.bar_off + 8 * (2 * p.stages + 3) + 16;
+    // aux_full, slice_full and the TMEM address slot; as deep a ring as fits
+    // (at least 2 stages)
+    auto layout = [&](int st) {
+      const size_t ring = (size_t)st * stage_bytes;
+      p.stages = st;
+      p.region = (uint32_t)((ring > sl_xs ? ring : sl_xs + 1023) & ~size_t(1023));
+      p.hc_off = p.region + (uint32_t)ls;
+      p.tok_off = p.hc_off + (uint32_t)hc;
+      p.bar_off = p.tok_off + 8 * LT_BM;
+      return 1024 + (size_t)p.bar_off + 8 * (2 * st + 3) + 16;
+    };
+    int st = per_cta < 6 ? (per_cta < 2 ? 2 : per_cta) : 6;
+    size_t smem = layout(st);
+    while (st > 2 && smem > kSmemBudget) smem = layout(--st);
     CUtensorMap mapWlat, mapHc, mapPart, mapPartSt, mapL, mapU, mapUbS;
     if (!cached_map_bf16_2d(&mapWlat, W_lat, (uint64_t)R, (uint64_t)D, (uint64_t)R, 64, LT_BK) ||
         !cached_map_plain_2d(&mapHc, hcache, 2, (uint64_t)R, (uint64_t)(N * B), (uint64_t)R, (uint32_t)t.w, LT_BM) ||
