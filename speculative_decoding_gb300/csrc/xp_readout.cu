@@ -158,7 +158,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], 2);  // one (release) arrive per CTA of the pair
     }
-    mbar_init(a_ready, 2 * RO_EPI_WARPS);
+    mbar_init(a_ready, 2);  // one (release) arrive per CTA of the pair
     mbar_init(drain, 1);
     mbar_init(&a_full[0], 1);
     mbar_init(&a_full[1], 1);
@@ -372,9 +372,11 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
         if (lane == 0) mbar_arrive(a_free);  // this warp is done reading the round
       }
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) arrive_leader(a_ready);
-      if (threadIdx.x == 64) XP_TRACE_MARK(2);
+      named_barrier_sync(2, 32 * RO_EPI_WARPS);
+      if (threadIdx.x == 64) {
+        arrive_leader(a_ready);
+        XP_TRACE_MARK(2);
+      }
     }
 
     float best = -INFINITY;
