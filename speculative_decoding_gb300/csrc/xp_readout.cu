@@ -183,6 +183,12 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   // pass) run ahead of the wait below.
   pdl_launch_dependents();
   if (warp != 0 && warp != RO_WARP_W2B && warp != RO_WARP_BASE) pdl_wait();
+  // Copies this CTA requested, for the drain before exit when a wait timed
+  // out (on the normal path every copy is consumed before the end)
+  int timed_out = 0;      // this thread saw a wait run out
+  uint32_t w2_armed = 0;  // phases of b_full[pid] a leader producer armed
+  int lat_issued = 0;     // latent rounds requested
+  int base_issued = 0;    // base tiles requested
   // the leader's copy of a barrier, as a shared::cluster address
   auto leader_bar = [](uint64_t* b) { return mapa_shared(smem_u32(b), 0u); };
   // arrive on the leader's copy of a barrier (locally in the leader)
@@ -208,7 +214,10 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       int ok = 1;
       if (lane == 0) {
         if (u >= 1 && !mbar_wait_cluster(&acc_full[pid], (u - 1) & 1)) ok = 0;
-        else if (rank == 0) mbar_arrive_expect_tx(&b_full[pid], 2u * (uint32_t)p.kch * RO_W2_BOX);
+        else if (rank == 0) {
+          mbar_arrive_expect_tx(&b_full[pid], 2u * (uint32_t)p.kch * RO_W2_BOX);
+          ++w2_armed;
+        }
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) {
         dead = true;
@@ -222,6 +231,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
     }
     pdl_wait();  // returns at once if already passed above
     if (dead && lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+    timed_out = dead;
     if (pid == 0 && lane == 0) XP_TRACE_MARK(7);
   } else if (warp == RO_WARP_BASE) {
     // ---------------- TMA producer: base tiles (two lanes, one box each) ----------------
@@ -254,6 +264,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       if (lane < nbox)
         tma_load_2d(sBase + (size_t)lane * RO_BASE_BOX, &mapLat, (RO_A_ROUND * r + lane) * 64, m_tile * RO_BM,
                     &a_full[r]);
+      lat_issued = r + 1;
     }
     {
       int ok = 1;
@@ -261,6 +272,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       a_dead = !__shfl_sync(0xffffffffu, ok, 0);
     }
     if (a_dead) {
+      timed_out = 1;
       if (lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
     } else {
       for (int t = 0; t < ntiles; ++t) {
@@ -272,9 +284,11 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
           else mbar_arrive_expect_tx(&base_full[bb], RO_BASE_TILE);
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          timed_out = 1;
           if (lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
           break;
         }
+        base_issued = t + 1;
         if (lane < 2)
           tma_load_2d_hint(sBase + (size_t)bb * RO_BASE_TILE + lane * RO_BASE_BOX, &mapBase, n0 + lane * 64,
                            m_tile * RO_BM, &base_full[bb], pol_base);
@@ -322,6 +336,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
         tc_commit_pair(&acc_full[a], 0x3);
       }
       if (dead) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+      timed_out = dead;
       XP_TRACE_MARK(4);
       tc_commit_pair(drain, 0x1);
       (void)mbar_wait(drain, 0);
@@ -346,6 +361,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       for (int r = 0; r < rounds; ++r) {
         if (ok && !mbar_wait(&a_full[r], 0)) {
           ok = false;
+          timed_out = 1;
           flag_error(p.hdr, XP_DEVERR_TIMEOUT);
         }
         if (ok) {
@@ -388,10 +404,12 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       const int n0 = (n_begin + t) * RO_BN + h * 64;
       if (!dead && !mbar_wait(&base_full[bb], kb & 1)) {
         dead = true;
+        timed_out = 1;
         flag_error(p.hdr, XP_DEVERR_TIMEOUT);
       }
       if (!dead && !mbar_wait(&acc_full[a], u & 1)) {
         dead = true;
+        timed_out = 1;
         flag_error(p.hdr, XP_DEVERR_TIMEOUT);
       }
       tc_fence_after();
@@ -433,7 +451,22 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
 
   __syncwarp();  // lane-0 roles rejoin their warps before any .aligned op
   tc_fence_before();
-  __syncthreads();
+  // After a timeout some copies this CTA requested may never have been
+  // consumed: each producer waits (bounded) for the last phase it armed on
+  // each of its barriers before the pair may exit.  Earlier phases of a
+  // barrier are complete: a phase is re-armed only after its previous one
+  // was consumed.  The peer's W2 halves count on the leader's b_full, and the
+  // peer cannot exit before the cluster barrier below.
+  if (__syncthreads_or(timed_out) && lane == 0) {
+    if ((warp == 0 || warp == RO_WARP_W2B) && w2_armed > 0)
+      (void)mbar_wait(&b_full[warp == 0 ? 0 : 1], (w2_armed - 1) & 1);
+    if (warp == RO_WARP_BASE) {
+      for (int r = 0; r < lat_issued; ++r) (void)mbar_wait(&a_full[r], 0);
+      for (int t = base_issued > RO_NBASE ? base_issued - RO_NBASE : 0; t < base_issued; ++t)
+        (void)mbar_wait(&base_full[t % RO_NBASE], (uint32_t)(t / RO_NBASE) & 1);
+    }
+  }
+  __syncwarp();
   // the leader's MMAs are complete (drain) and no remote arrive is in flight
   // once both CTAs are here
   cluster_sync();
