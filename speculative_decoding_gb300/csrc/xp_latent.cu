@@ -146,6 +146,9 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) XP_TRACE_MARK(1);
   pdl_launch_dependents();
+  // copies requested, for the drain before exit after a timed-out wait
+  int timed_out = 0, issued = 0;
+  bool aux_issued = false, slices_issued = false;
 
   if (warp == 0) {
     // Nothing this warp reads is written by the preceding kernels, so it
@@ -159,6 +162,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     // two boxes: the hidden-cache slice and the mixer weights of the slice
     // (the whole [B][B] square of L for these w channels)
     auto aux_copies = [&]() {
+      aux_issued = true;
       if (lane == 0) {
         mbar_arrive_expect_tx(aux_full, (uint32_t)(p.B * p.B * p.w * 4) + (uint32_t)(LT_BM * p.w * 2));
         tma_load_2d(smem + p.hc_off, &mapHc, col0, mt * p.bpt * p.B, aux_full);
@@ -183,14 +187,16 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
+        timed_out = 1;
         if (lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
         break;
       }
+      issued = i + 1;
       if (lane < p.tn / 64)
         tma_load_2d_hint(smem + (size_t)s * stage_bytes + LT_A_CHUNK + lane * LT_BOX, &mapWlat,
                          nt * p.tn + lane * 64, (c0 + i) * LT_BK, &full[s], pol);
     }
-    if (nck <= 1) aux_copies();
+    if (nck <= 1 && !timed_out) aux_copies();
     if (lane == 0) XP_TRACE_MARK(3);
   } else if (warp == 1) {
     if (lane == 0) {
@@ -215,6 +221,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
         tc_commit(&empty[s]);
       }
       if (dead) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+      timed_out = dead;
       tc_commit(acc_full);
       XP_TRACE_MARK(8);
     }
@@ -275,6 +282,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
       }
     }
     if (dead) {
+      timed_out = 1;
       flag_error(p.hdr, XP_DEVERR_TIMEOUT);
       cp_async_wait_all();
     } else {
@@ -287,7 +295,10 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
   // row per thread, 128-byte swizzle: conflict-free) -> TMA stores into the
   // partial buffer
   if (warp >= 2) {
-    if (!mbar_wait(acc_full, 0)) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+    if (!mbar_wait(acc_full, 0)) {
+      timed_out = 1;
+      flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+    }
     tc_fence_after();
     if (threadIdx.x == 64) XP_TRACE_MARK(9);
     const int q = warp & 3, row = q * 32 + lane;
@@ -334,8 +345,10 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) {
+      timed_out = 1;
       if (lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
     } else {
+      slices_issued = true;
       if (lane < p.S)
         tma_load_2d(slices + (size_t)lane * LT_BM * p.w, &mapPart, col0,
                     (int)((int64_t)lane * p.rows_pad + (int64_t)mt * LT_BM), slice_full);
@@ -353,7 +366,10 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
 
   if (warp >= 2) {
     const int et = threadIdx.x - 64;
-    if (!mbar_wait(slice_full, 0) || !mbar_wait(aux_full, 0)) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+    if (!mbar_wait(slice_full, 0) || !mbar_wait(aux_full, 0)) {
+      timed_out = 1;
+      flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+    }
     // ---- epilogue 2: x = hcache + sum of the S partials (slice order) for
     // this CTA's columns of all rows, four columns per item
     const int wq = p.w / 4, items = LT_BM * wq;
@@ -413,6 +429,16 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     }
   }
   tc_fence_before();
+  // After a timed-out wait, warp 0 waits (bounded) for every copy it may
+  // still have in flight into this CTA's shared memory before the CTA exits
+  // (earlier phases of a ring slot are complete: a slot is re-armed only
+  // after its previous phase was consumed)
+  if (__syncthreads_or(timed_out) && threadIdx.x == 0) {
+    for (int j = issued > p.stages ? issued - p.stages : 0; j < issued; ++j)
+      (void)mbar_wait(&full[j % p.stages], (uint32_t)(j / p.stages) & 1);
+    if (aux_issued) (void)mbar_wait(aux_full, 0);
+    if (slices_issued) (void)mbar_wait(slice_full, 0);
+  }
   __syncthreads();
   if (threadIdx.x == 0) XP_TRACE_MARK(14);
   if (warp == 1) {
@@ -466,6 +492,7 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) XP_TRACE_MARK(17);
   pdl_launch_dependents();
+  int timed_out = 0, issued = 0;  // for the drain before exit after a timed-out wait
 
   if (warp == 0) {
     // lane 0 arms the stage; lanes 0, 1, 2 issue the ub, Wg and Wu boxes.
@@ -478,6 +505,7 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
     }
     const uint64_t pol = policy_evict_last();  // every pass re-reads Wg, Wu
     const int pre = p.chunks < p.stages ? p.chunks : p.stages;
+    issued = pre;
     for (int i = 0; i < pre; ++i) {
       uint8_t* dst = smem + (size_t)i * stage_bytes;
       if (lane == 0) mbar_arrive_expect_tx(&full[i], stage_bytes);
@@ -498,9 +526,11 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
+        timed_out = 1;
         if (lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
         break;
       }
+      issued = i + 1;
       uint8_t* dst = smem + (size_t)s * stage_bytes;
       if (lane == 0) tma_load_2d(dst, &mapUb, i * LT_BK, mt * LT_BM, &full[s]);
       if (lane == 1) tma_load_2d_hint(dst + LT_A_CHUNK, &mapWg, ht * 64, i * LT_BK, &full[s], pol);
@@ -530,12 +560,16 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
         tc_commit(&empty[s]);
       }
       if (dead) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+      timed_out = dead;
       tc_commit(acc_full);
       XP_TRACE_MARK(20);
     }
   } else {
     pdl_wait();
-    if (!mbar_wait(acc_full, 0)) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+    if (!mbar_wait(acc_full, 0)) {
+      timed_out = 1;
+      flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+    }
     tc_fence_after();
     if (threadIdx.x == 64) XP_TRACE_MARK(21);
     const int q = warp & 3;
@@ -563,6 +597,10 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
     if (threadIdx.x == 64) XP_TRACE_MARK(22);
   }
   tc_fence_before();
+  // after a timed-out wait: the ring's copies still in flight land before exit
+  if (__syncthreads_or(timed_out) && threadIdx.x == 0)
+    for (int j = issued > p.stages ? issued - p.stages : 0; j < issued; ++j)
+      (void)mbar_wait(&full[j % p.stages], (uint32_t)(j / p.stages) & 1);
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -634,6 +672,7 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) XP_TRACE_MARK(33);
   pdl_launch_dependents();
+  int timed_out = 0, issued = 0;  // for the drain before exit after a timed-out wait
 
   if (warp == 0) {
     // lane 0 arms the stage; lane 0 issues the m box, lanes 1.. the Wd boxes.
@@ -647,6 +686,7 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
     }
     const uint64_t pol = policy_evict_last();  // every pass re-reads Wd
     const int pre = nck < p.stages ? nck : p.stages;
+    issued = pre;
     for (int i = 0; i < pre; ++i) {
       uint8_t* dst = smem + (size_t)i * stage_bytes;
       if (lane == 0) mbar_arrive_expect_tx(&full[i], stage_bytes);
@@ -671,9 +711,11 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
+        timed_out = 1;
         if (lane == 0) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
         break;
       }
+      issued = i + 1;
       uint8_t* dst = smem + (size_t)s * stage_bytes;
       if (lane == 0) tma_load_2d(dst, &mapM, (c0 + i) * LT_BK, mt * LT_BM, &full[s]);
       if (lane >= 1 && lane <= p.tn / 64)
@@ -703,12 +745,16 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
         tc_commit(&empty[s]);
       }
       if (dead) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+      timed_out = dead;
       tc_commit(acc_full);
       XP_TRACE_MARK(32 + 8);
     }
   } else {
     pdl_wait();
-    if (!mbar_wait(acc_full, 0)) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+    if (!mbar_wait(acc_full, 0)) {
+      timed_out = 1;
+      flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+    }
     tc_fence_after();
     if (threadIdx.x == 64) XP_TRACE_MARK(41);
     const int q = warp & 3, row = q * 32 + lane;
@@ -734,7 +780,10 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
   if (warp >= 2) {
     const int et = threadIdx.x - 64;
     const int wq = p.w / 4, items = LT_BM * wq;
-    if (!mbar_wait(aux_full, 0)) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+    if (!mbar_wait(aux_full, 0)) {
+      timed_out = 1;
+      flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+    }
     for (int i0 = et; i0 < items; i0 += 256) {
       float4 v[2][LT_MAX_S], uu[2];
       int64_t dst[2];
@@ -773,6 +822,14 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
     }
     if (et == 127) XP_TRACE_MARK(44);
   }
+  // after a timed-out wait: the copies still in flight land before exit (the
+  // residual box is always requested)
+  if (__syncthreads_or(timed_out) && threadIdx.x == 0) {
+    for (int j = issued > p.stages ? issued - p.stages : 0; j < issued; ++j)
+      (void)mbar_wait(&full[j % p.stages], (uint32_t)(j / p.stages) & 1);
+    (void)mbar_wait(aux_full, 0);
+  }
+  __syncwarp();
   cluster_sync_relaxed();  // the peers have finished reading this CTA's partial sums
   if (threadIdx.x == 0) XP_TRACE_MARK(45);
   if (warp == 1) {
