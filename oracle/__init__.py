@@ -76,8 +76,12 @@ def lib():
         L.orc_readout_bias.argtypes = [_u16p, _u16p, _i64, _i64, _i64, _u16p]
         L.orc_jacobi_pass.argtypes = [_i64p, _i64p, _u16p, _u16p, _u16p, _f32p, _u16p, _u16p, _u16p,
                                       _u16p, _u16p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64p]
+        L.orc_latent_ex.argtypes = [_i64p, _i64p, _u16p, _u16p, _u16p, _f32p, _u16p, _u16p, _u16p, _u16p,
+                                    _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f64p, _i64, _i64]
+        L.orc_jacobi_pass_ex.argtypes = [_i64p, _i64p, _u16p, _u16p, _u16p, _f32p, _u16p, _u16p, _u16p,
+                                         _u16p, _u16p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64p]
         for name in ("orc_add_argmax", "orc_topc_argmax", "orc_latent", "orc_row_logits",
-                     "orc_readout_bias", "orc_jacobi_pass"):
+                     "orc_readout_bias", "orc_jacobi_pass", "orc_latent_ex", "orc_jacobi_pass_ex"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -145,10 +149,12 @@ def topc_argmax(base_c: np.ndarray, bias_c: np.ndarray, cand: np.ndarray, blk: n
                                  _p(cand, np.int64, _i64p), rows, C, _p(blk, np.int64, _i64p), N, B))
 
 
-def latent(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, blocks=None, want_u=False):
+def latent(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, blocks=None, want_u=False, do_mlp=True):
     """Latent stage.  Returns lat_out [N, B-1, R] bf16 bits (and the mixer
     output u [N, B, R] float64 when ``want_u``).  ``blocks=(lo, hi)`` limits the
-    work to blocks lo..hi-1; the other rows of the outputs are left zero."""
+    work to blocks lo..hi-1; the other rows of the outputs are left zero.
+    ``do_mlp`` False selects the GEMM schedule of ``xpress_latent_pass``
+    (bf16 u handed back, then u @ wgu_t, silu_and_mul, addmm_ in bf16)."""
     N, B = blk.shape
     V, D = E.shape
     R = W_lat.shape[1]
@@ -158,12 +164,12 @@ def latent(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, blocks=None, want_u=False)
     lo, hi = blocks if blocks is not None else (0, N)
     lat = np.zeros((N, B - 1, R), np.uint16)
     u = np.zeros((N, B, R), np.float64) if want_u else None
-    _check(lib().orc_latent(_p(blk, np.int64, _i64p), _p(am1, np.int64, _i64p),
-                            _p(hcache, np.uint16, _u16p), _p(E, np.uint16, _u16p),
-                            _p(W_lat, np.uint16, _u16p), _p(L, np.float32, _f32p),
-                            _p(Wg, np.uint16, _u16p), _p(Wu, np.uint16, _u16p), _p(Wd, np.uint16, _u16p),
-                            _p(lat, np.uint16, _u16p), N, B, V, D, R, H,
-                            _p(u, np.float64, _f64p) if want_u else None, lo, hi))
+    _check(lib().orc_latent_ex(_p(blk, np.int64, _i64p), _p(am1, np.int64, _i64p),
+                               _p(hcache, np.uint16, _u16p), _p(E, np.uint16, _u16p),
+                               _p(W_lat, np.uint16, _u16p), _p(L, np.float32, _f32p),
+                               _p(Wg, np.uint16, _u16p), _p(Wu, np.uint16, _u16p), _p(Wd, np.uint16, _u16p),
+                               _p(lat, np.uint16, _u16p), N, B, V, D, R, H, 1 if do_mlp else 0,
+                               _p(u, np.float64, _f64p) if want_u else None, lo, hi))
     return (lat, u) if want_u else lat
 
 
@@ -188,20 +194,21 @@ def row_logits(lat_row: np.ndarray, W2: np.ndarray, base_row: np.ndarray) -> np.
     return out
 
 
-def jacobi_pass(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, W2, base) -> int:
-    """One pass in place on ``blk``; returns the number of slots that changed."""
+def jacobi_pass(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, W2, base, do_mlp=True) -> int:
+    """One pass in place on ``blk``; returns the number of slots that changed.
+    ``do_mlp`` as in ``latent``."""
     N, B = blk.shape
     V, D = E.shape
     R = W_lat.shape[1]
     H = Wg.shape[1]
     changed = np.zeros(1, np.int64)
-    _check(lib().orc_jacobi_pass(_p(blk, np.int64, _i64p), _p(am1, np.int64, _i64p),
-                                 _p(hcache, np.uint16, _u16p), _p(E, np.uint16, _u16p),
-                                 _p(W_lat, np.uint16, _u16p), _p(L, np.float32, _f32p),
-                                 _p(Wg, np.uint16, _u16p), _p(Wu, np.uint16, _u16p),
-                                 _p(Wd, np.uint16, _u16p), _p(W2, np.uint16, _u16p),
-                                 _p(base, np.uint16, _u16p), base.strides[0] // 2,
-                                 N, B, V, D, R, H, _p(changed, np.int64, _i64p)))
+    _check(lib().orc_jacobi_pass_ex(_p(blk, np.int64, _i64p), _p(am1, np.int64, _i64p),
+                                    _p(hcache, np.uint16, _u16p), _p(E, np.uint16, _u16p),
+                                    _p(W_lat, np.uint16, _u16p), _p(L, np.float32, _f32p),
+                                    _p(Wg, np.uint16, _u16p), _p(Wu, np.uint16, _u16p),
+                                    _p(Wd, np.uint16, _u16p), _p(W2, np.uint16, _u16p),
+                                    _p(base, np.uint16, _u16p), base.strides[0] // 2,
+                                    N, B, V, D, R, H, 1 if do_mlp else 0, _p(changed, np.int64, _i64p)))
     return int(changed[0])
 
 

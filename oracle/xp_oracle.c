@@ -23,6 +23,10 @@
  *       (slot 0 gathers am1[n]); u[b] = sum_{j<=b} L[b,j,:] * x[j];
  *       ub = bf16(u); m = bf16(silu(ub@Wg) * (ub@Wu)); y = u + m@Wd (residual
  *       on the unrounded u); lat_out[n, b-1] = bf16(y) for b = 1..B-1.
+ *   xpress_latent_pass with do_mlp False (the GEMM schedule): the kernel
+ *       stops after the mixer and hands back bf16(u); the caller then runs
+ *       gu = u @ wgu_t (a bf16 matmul, [Wg | Wu] side by side),
+ *       m = silu_and_mul(gu) and u.addmm_(m, wd_t) on the bf16 u.
  *   fused_topc_argmax_to_blk: the top-C variant over gathered candidates.
  *
  * Readings where the pages leave a step open (each is listed in the design
@@ -193,11 +197,12 @@ static double silu_times(double g, double v) { return g * (1.0 / (1.0 + exp(-g))
 
 /* One block n.  x, u: B*R doubles of scratch; ub: R; m: H.  Writes
  * lat_out[n, 0..B-2, :] and, when u_out is given, u_out[n, :, :] (the mixer
- * output, before the MLP). */
+ * output, before the MLP).  do_mlp selects the MLP schedule: 1 the in-kernel
+ * MLP (fp32 g, v and residual), 0 the GEMM schedule (bf16 g, v and residual). */
 static int latent_block(int64_t n, const int64_t* blk, const int64_t* am1, const uint16_t* hcache,
                         const uint16_t* E, const uint16_t* W_lat, const float* L, const uint16_t* Wg,
                         const uint16_t* Wu, const uint16_t* Wd, uint16_t* lat_out, int64_t B,
-                        int64_t V, int64_t D, int64_t R, int64_t H, double* u_out, double* x,
+                        int64_t V, int64_t D, int64_t R, int64_t H, int do_mlp, double* u_out, double* x,
                         double* u, double* ubd, double* m) {
     /* gather + projection + hidden cache */
     for (int64_t b = 0; b < B; ++b) {
@@ -229,6 +234,28 @@ static int latent_block(int64_t n, const int64_t* blk, const int64_t* am1, const
     for (int64_t b = 1; b < B; ++b) {
         const double* ub = u + b * R;
         for (int64_t r = 0; r < R; ++r) ubd[r] = bf(bf16_from_double(ub[r]));
+        if (!do_mlp) {
+            /* GEMM schedule: the latent kernel's output is bf16(u) = ubd.
+             * gu = bf16(ubd @ [Wg | Wu]): each half rounded to bf16 (the
+             * matmul returns a bf16 tensor); silu_and_mul: m = bf16(silu(g) * v)
+             * from the bf16 g and v; addmm_ into the bf16 u: the product is
+             * added to ubd and the sum rounded to bf16 once. */
+            for (int64_t h = 0; h < H; ++h) {
+                double g = 0.0, v = 0.0;
+                for (int64_t r = 0; r < R; ++r) {
+                    g += ubd[r] * bf(Wg[r * H + h]);
+                    v += ubd[r] * bf(Wu[r * H + h]);
+                }
+                m[h] = bf(bf16_from_double(silu_times(bf(bf16_from_double(g)), bf(bf16_from_double(v)))));
+            }
+            uint16_t* out = lat_out + (n * (B - 1) + (b - 1)) * R;
+            for (int64_t r = 0; r < R; ++r) {
+                double y = ubd[r];
+                for (int64_t h = 0; h < H; ++h) y += m[h] * bf(Wd[h * R + r]);
+                out[r] = bf16_from_double(y);
+            }
+            continue;
+        }
         for (int64_t h = 0; h < H; ++h) {
             double g = 0.0, v = 0.0;
             for (int64_t r = 0; r < R; ++r) {
@@ -248,11 +275,12 @@ static int latent_block(int64_t n, const int64_t* blk, const int64_t* am1, const
 }
 
 /* Latent for blocks [n_lo, n_hi).  lat_out is the full [N, B-1, R] buffer;
- * u_out (nullable) the full [N, B, R] buffer of mixer outputs in double. */
-int orc_latent(const int64_t* blk, const int64_t* am1, const uint16_t* hcache, const uint16_t* E,
-               const uint16_t* W_lat, const float* L, const uint16_t* Wg, const uint16_t* Wu,
-               const uint16_t* Wd, uint16_t* lat_out, int64_t N, int64_t B, int64_t V, int64_t D,
-               int64_t R, int64_t H, double* u_out, int64_t n_lo, int64_t n_hi) {
+ * u_out (nullable) the full [N, B, R] buffer of mixer outputs in double;
+ * do_mlp as in latent_block. */
+int orc_latent_ex(const int64_t* blk, const int64_t* am1, const uint16_t* hcache, const uint16_t* E,
+                  const uint16_t* W_lat, const float* L, const uint16_t* Wg, const uint16_t* Wu,
+                  const uint16_t* Wd, uint16_t* lat_out, int64_t N, int64_t B, int64_t V, int64_t D,
+                  int64_t R, int64_t H, int64_t do_mlp, double* u_out, int64_t n_lo, int64_t n_hi) {
     if (!blk || !am1 || !hcache || !E || !W_lat || !L || !Wg || !Wu || !Wd || !lat_out) return ORC_ERR_ARG;
     if (N < 1 || B < 2 || V < 1 || D < 1 || R < 1 || H < 1) return ORC_ERR_ARG;
     if (n_lo < 0 || n_hi > N || n_lo > n_hi) return ORC_ERR_ARG;
@@ -266,7 +294,7 @@ int orc_latent(const int64_t* blk, const int64_t* am1, const uint16_t* hcache, c
 #pragma omp for schedule(dynamic, 1)
         for (int64_t n = n_lo; n < n_hi; ++n) {
             int st = latent_block(n, blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, lat_out, B, V, D, R, H,
-                                  u_out, x, u, ubd, m);
+                                  do_mlp != 0, u_out, x, u, ubd, m);
             if (st != ORC_OK) {
 #pragma omp critical
                 status = st;
@@ -278,6 +306,15 @@ int orc_latent(const int64_t* blk, const int64_t* am1, const uint16_t* hcache, c
         free(m);
     }
     return status;
+}
+
+/* The in-kernel MLP schedule. */
+int orc_latent(const int64_t* blk, const int64_t* am1, const uint16_t* hcache, const uint16_t* E,
+               const uint16_t* W_lat, const float* L, const uint16_t* Wg, const uint16_t* Wu,
+               const uint16_t* Wd, uint16_t* lat_out, int64_t N, int64_t B, int64_t V, int64_t D,
+               int64_t R, int64_t H, double* u_out, int64_t n_lo, int64_t n_hi) {
+    return orc_latent_ex(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, lat_out, N, B, V, D, R, H, 1, u_out, n_lo,
+                         n_hi);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -336,10 +373,11 @@ int orc_readout_bias(const uint16_t* lat, const uint16_t* W2, int64_t rows, int6
 /* *changed (nullable) receives the number of slots whose token changed.    */
 /* ------------------------------------------------------------------------ */
 
-int orc_jacobi_pass(int64_t* blk, const int64_t* am1, const uint16_t* hcache, const uint16_t* E,
-                    const uint16_t* W_lat, const float* L, const uint16_t* Wg, const uint16_t* Wu,
-                    const uint16_t* Wd, const uint16_t* W2, const uint16_t* base, int64_t ld_base,
-                    int64_t N, int64_t B, int64_t V, int64_t D, int64_t R, int64_t H, int64_t* changed) {
+int orc_jacobi_pass_ex(int64_t* blk, const int64_t* am1, const uint16_t* hcache, const uint16_t* E,
+                       const uint16_t* W_lat, const float* L, const uint16_t* Wg, const uint16_t* Wu,
+                       const uint16_t* Wd, const uint16_t* W2, const uint16_t* base, int64_t ld_base,
+                       int64_t N, int64_t B, int64_t V, int64_t D, int64_t R, int64_t H, int64_t do_mlp,
+                       int64_t* changed) {
     if (!blk || !W2 || !base || ld_base < V) return ORC_ERR_ARG;
     int64_t rows = N * (B - 1);
     if (!all_finite_bf16(base, rows, V, ld_base)) return ORC_ERR_NONFINITE;
@@ -352,7 +390,7 @@ int orc_jacobi_pass(int64_t* blk, const int64_t* am1, const uint16_t* hcache, co
         free(fresh);
         return ORC_ERR_ARG;
     }
-    int st = orc_latent(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, lat, N, B, V, D, R, H, NULL, 0, N);
+    int st = orc_latent_ex(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, lat, N, B, V, D, R, H, do_mlp, NULL, 0, N);
     if (st == ORC_OK) st = orc_readout_bias(lat, W2, rows, R, V, bias);
     if (st == ORC_OK) {
 #pragma omp parallel for schedule(dynamic, 1)
@@ -369,4 +407,12 @@ int orc_jacobi_pass(int64_t* blk, const int64_t* am1, const uint16_t* hcache, co
     free(bias);
     free(fresh);
     return st;
+}
+
+int orc_jacobi_pass(int64_t* blk, const int64_t* am1, const uint16_t* hcache, const uint16_t* E,
+                    const uint16_t* W_lat, const float* L, const uint16_t* Wg, const uint16_t* Wu,
+                    const uint16_t* Wd, const uint16_t* W2, const uint16_t* base, int64_t ld_base,
+                    int64_t N, int64_t B, int64_t V, int64_t D, int64_t R, int64_t H, int64_t* changed) {
+    return orc_jacobi_pass_ex(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, W2, base, ld_base, N, B, V, D, R, H, 1,
+                              changed);
 }
