@@ -171,6 +171,29 @@ XP_API xp_status xp_latent_pass(const int64_t* d_blk, const int64_t* d_am1, cons
                          int64_t H, void* d_workspace, size_t workspace_bytes, xp_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * xp_latent_pass_ex -- xp_latent_pass with the MLP schedule selectable.
+ * Pages: xpress_latent_pass, argument do_mlp.
+ *
+ *   do_mlp = 1: the in-kernel MLP, exactly xp_latent_pass.
+ *   do_mlp = 0: the GEMM schedule.  The kernel stops after the mixer and
+ *     hands back ub = bf16(u); the caller's GEMMs then run on that bf16
+ *     tensor, with [Wg | Wu] side by side as wgu_t:
+ *       g = bf16(ub @ Wg);  v = bf16(ub @ Wu)                 (u @ wgu_t)
+ *       m = bf16(g * sigmoid(g) * v)                           (silu_and_mul)
+ *       lat_out[n,b-1,:] = bf16(float(ub) + m @ Wd)            (u.addmm_(m, wd_t))
+ *     i.e. g and v are rounded before the SiLU and the residual is bf16(u).
+ *   Here both schedules run in the same kernels (the roundings are applied
+ *   in their epilogues); any other do_mlp value is XP_ERR_SHAPE.
+ * Arguments, constraints and workspace as xp_latent_pass.
+ * ---------------------------------------------------------------------- */
+XP_API xp_status xp_latent_pass_ex(const int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_hcache,
+                                   const xp_bf16* d_E, const xp_bf16* d_W_lat, const float* d_L,
+                                   const xp_bf16* d_Wg, const xp_bf16* d_Wu, const xp_bf16* d_Wd,
+                                   xp_bf16* d_lat_out, int64_t N, int64_t B, int64_t V, int64_t D, int64_t R,
+                                   int64_t H, int32_t do_mlp, void* d_workspace, size_t workspace_bytes,
+                                   xp_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * xp_readout_argmax -- the readout matmul with the add + argmax fused into
  * its epilogue (the caller's `lat_out @ W2` followed by fused_add_argmax_to_blk,
  * without the bias or the logits ever reaching memory):
@@ -211,6 +234,16 @@ XP_API xp_status xp_jacobi_pass(int64_t* d_blk, const int64_t* d_am1, const xp_b
                          int64_t B, int64_t V, int64_t D, int64_t R, int64_t H,
                          int32_t* d_changed, void* d_workspace, size_t workspace_bytes,
                          xp_stream_t stream);
+
+/* xp_jacobi_pass_ex -- xp_jacobi_pass with the latent stage's MLP schedule
+ * selectable: do_mlp as in xp_latent_pass_ex (1 = xp_jacobi_pass). */
+XP_API xp_status xp_jacobi_pass_ex(int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_hcache,
+                                   const xp_bf16* d_E, const xp_bf16* d_W_lat, const float* d_L,
+                                   const xp_bf16* d_Wg, const xp_bf16* d_Wu, const xp_bf16* d_Wd,
+                                   const xp_bf16* d_W2, const xp_bf16* d_base, int64_t ld_base, int64_t N,
+                                   int64_t B, int64_t V, int64_t D, int64_t R, int64_t H, int32_t do_mlp,
+                                   int32_t* d_changed, void* d_workspace, size_t workspace_bytes,
+                                   xp_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * xp_jacobi_fixpoint -- Jacobi passes to the fixpoint, without a host

@@ -150,6 +150,16 @@ xp_status xp_latent_pass(const int64_t* d_blk, const int64_t* d_am1, const xp_bf
                          const xp_bf16* d_W_lat, const float* d_L, const xp_bf16* d_Wg, const xp_bf16* d_Wu,
                          const xp_bf16* d_Wd, xp_bf16* d_lat_out, int64_t N, int64_t B, int64_t V, int64_t D,
                          int64_t R, int64_t H, void* d_workspace, size_t workspace_bytes, xp_stream_t stream) {
+  return xp_latent_pass_ex(d_blk, d_am1, d_hcache, d_E, d_W_lat, d_L, d_Wg, d_Wu, d_Wd, d_lat_out, N, B, V, D, R, H,
+                           1, d_workspace, workspace_bytes, stream);
+}
+
+xp_status xp_latent_pass_ex(const int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_hcache,
+                            const xp_bf16* d_E, const xp_bf16* d_W_lat, const float* d_L, const xp_bf16* d_Wg,
+                            const xp_bf16* d_Wu, const xp_bf16* d_Wd, xp_bf16* d_lat_out, int64_t N, int64_t B,
+                            int64_t V, int64_t D, int64_t R, int64_t H, int32_t do_mlp, void* d_workspace,
+                            size_t workspace_bytes, xp_stream_t stream) {
+  if (do_mlp != 0 && do_mlp != 1) return XP_ERR_SHAPE;
   xp_status st = check_latent_args(d_blk, d_am1, d_hcache, d_E, d_W_lat, d_L, d_Wg, d_Wu, d_Wd, N, B, V, D, R, H);
   if (st != XP_OK || N == 0) return st;
   if (!d_lat_out || !d_workspace) return XP_ERR_NULL;
@@ -159,7 +169,7 @@ xp_status xp_latent_pass(const int64_t* d_blk, const int64_t* d_am1, const xp_bf
   st = check_device();
   if (st != XP_OK) return st;
   return xp::launch_latent(d_blk, d_am1, d_hcache, d_E, d_W_lat, d_L, d_Wg, d_Wu, d_Wd, d_lat_out, N, B, V, D, R, H,
-                           d_workspace, (cudaStream_t)stream);
+                           d_workspace, (cudaStream_t)stream, nullptr, do_mlp != 0);
 }
 
 size_t xp_jacobi_workspace_size(int64_t N, int64_t B, int64_t V, int64_t D, int64_t R, int64_t H) {
@@ -173,6 +183,16 @@ xp_status xp_jacobi_pass(int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_
                          const xp_bf16* d_Wd, const xp_bf16* d_W2t, const xp_bf16* d_base, int64_t ld_base, int64_t N,
                          int64_t B, int64_t V, int64_t D, int64_t R, int64_t H, int32_t* d_changed,
                          void* d_workspace, size_t workspace_bytes, xp_stream_t stream) {
+  return xp_jacobi_pass_ex(d_blk, d_am1, d_hcache, d_E, d_W_lat, d_L, d_Wg, d_Wu, d_Wd, d_W2t, d_base, ld_base, N, B,
+                           V, D, R, H, 1, d_changed, d_workspace, workspace_bytes, stream);
+}
+
+xp_status xp_jacobi_pass_ex(int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_hcache, const xp_bf16* d_E,
+                            const xp_bf16* d_W_lat, const float* d_L, const xp_bf16* d_Wg, const xp_bf16* d_Wu,
+                            const xp_bf16* d_Wd, const xp_bf16* d_W2t, const xp_bf16* d_base, int64_t ld_base,
+                            int64_t N, int64_t B, int64_t V, int64_t D, int64_t R, int64_t H, int32_t do_mlp,
+                            int32_t* d_changed, void* d_workspace, size_t workspace_bytes, xp_stream_t stream) {
+  if (do_mlp != 0 && do_mlp != 1) return XP_ERR_SHAPE;
   xp_status st = check_latent_args(d_blk, d_am1, d_hcache, d_E, d_W_lat, d_L, d_Wg, d_Wu, d_Wd, N, B, V, D, R, H);
   if (st != XP_OK || N == 0) return st;
   if (ld_base < V) return XP_ERR_SHAPE;
@@ -184,7 +204,7 @@ xp_status xp_jacobi_pass(int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_
   if (st != XP_OK) return st;
   uint16_t* lat = reinterpret_cast<uint16_t*>(static_cast<char*>(d_workspace) + lay.lat);
   st = xp::launch_latent(d_blk, d_am1, d_hcache, d_E, d_W_lat, d_L, d_Wg, d_Wu, d_Wd, lat, N, B, V, D, R, H,
-                         d_workspace, (cudaStream_t)stream);
+                         d_workspace, (cudaStream_t)stream, nullptr, do_mlp != 0);
   if (st != XP_OK) return st;
   return xp::launch_readout_argmax(lat, d_W2t, d_base, ld_base, N * (B - 1), V, R, d_blk, B, d_changed, d_workspace,
                                    (cudaStream_t)stream);

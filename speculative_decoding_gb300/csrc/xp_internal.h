@@ -31,6 +31,7 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
 xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* hcache, const uint16_t* E,
                         const uint16_t* W_lat, const float* L, const uint16_t* Wg, const uint16_t* Wu,
                         const uint16_t* Wd, uint16_t* lat_out, int64_t N, int64_t B, int64_t V, int64_t D, int64_t R,
-                        int64_t H, void* ws, cudaStream_t stream, const uint32_t* skip = nullptr);
+                        int64_t H, void* ws, cudaStream_t stream, const uint32_t* skip = nullptr,
+                        bool do_mlp = true);
 
 }  // namespace xp

@@ -457,6 +457,9 @@ struct UpParams {
   const uint32_t* skip;  // nullable: see pass_skipped
 };
 
+// kGemm: the GEMM schedule (g and v rounded to bf16 before the SiLU, as the
+// bf16 u @ wgu_t returns them); else the in-kernel MLP (fp32 g and v)
+template <bool kGemm>
 __global__ void __launch_bounds__(LT_THREADS, 1)
 mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__ CUtensorMap mapWg,
               const __grid_constant__ CUtensorMap mapWu, const UpParams p) {
@@ -584,9 +587,18 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float g0 = __uint_as_float(g[2 * e]), g1 = __uint_as_float(g[2 * e + 1]);
-          const float m0 = __fdividef(g0, 1.f + __expf(-g0)) * __uint_as_float(v[2 * e]);
-          const float m1 = __fdividef(g1, 1.f + __expf(-g1)) * __uint_as_float(v[2 * e + 1]);
+          float g0 = __uint_as_float(g[2 * e]), g1 = __uint_as_float(g[2 * e + 1]);
+          float v0 = __uint_as_float(v[2 * e]), v1 = __uint_as_float(v[2 * e + 1]);
+          if (kGemm) {
+            // the GEMM schedule's u @ wgu_t returns bf16: round g and v first
+            const uint32_t gq = f32x2_to_bf16x2(g0, g1), vq = f32x2_to_bf16x2(v0, v1);
+            g0 = bf16lo_to_f32(gq);
+            g1 = bf16hi_to_f32(gq);
+            v0 = bf16lo_to_f32(vq);
+            v1 = bf16hi_to_f32(vq);
+          }
+          const float m0 = __fdividef(g0, 1.f + __expf(-g0)) * v0;
+          const float m1 = __fdividef(g1, 1.f + __expf(-g1)) * v1;
           w[e] = f32x2_to_bf16x2(m0, m1);
         }
         uint4* dst = reinterpret_cast<uint4*>(p.m + (int64_t)row * p.H + ht * 64 + c * 32);
@@ -625,6 +637,9 @@ struct DownParams {
   const uint32_t* skip;  // nullable: see pass_skipped
 };
 
+// kGemm: the GEMM schedule (the residual is bf16(u): addmm_ into the bf16 u);
+// else the in-kernel MLP (the fp32 residual u)
+template <bool kGemm>
 __global__ void __launch_bounds__(LT_THREADS, 2)
 mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant__ CUtensorMap mapWd,
                 const __grid_constant__ CUtensorMap mapU, const DownParams p) {
@@ -798,6 +813,10 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
         on[h] = it < items && grow < rows && b >= 1 && col < p.R;
         dst[h] = ((int64_t)n * (p.B - 1) + b - 1) * p.R + col;
         uu[h] = on[h] ? *reinterpret_cast<const float4*>(us + rr * p.w + 4 * gg) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (kGemm) {
+          const uint32_t lo = f32x2_to_bf16x2(uu[h].x, uu[h].y), hi = f32x2_to_bf16x2(uu[h].z, uu[h].w);
+          uu[h] = make_float4(bf16lo_to_f32(lo), bf16hi_to_f32(lo), bf16lo_to_f32(hi), bf16hi_to_f32(hi));
+        }
 #pragma unroll
         for (int q = 0; q < LT_MAX_S; ++q)
           v[h][q] = (on[h] && q < p.S) ? ld_dsmem_v4(red + rr * ld + c_lo + 4 * gg, (uint32_t)q)
@@ -883,7 +902,7 @@ constexpr size_t kSmemBudget = 226 * 1024;
 xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* hcache, const uint16_t* E,
                         const uint16_t* W_lat, const float* L, const uint16_t* Wg, const uint16_t* Wu,
                         const uint16_t* Wd, uint16_t* lat_out, int64_t N, int64_t B, int64_t V, int64_t D, int64_t R,
-                        int64_t H, void* ws, cudaStream_t stream, const uint32_t* skip) {
+                        int64_t H, void* ws, cudaStream_t stream, const uint32_t* skip, bool do_mlp) {
   if (N <= 0) return XP_OK;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return XP_ERR_LAUNCH;
@@ -900,8 +919,9 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
                                   max_smem - (int)fa.sharedSizeBytes) == cudaSuccess &&
              cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
     };
-    if (!allow((const void*)proj_mix_kernel) || !allow((const void*)mlp_up_kernel) ||
-        !allow((const void*)mlp_down_kernel))
+    if (!allow((const void*)proj_mix_kernel) || !allow((const void*)mlp_up_kernel<false>) ||
+        !allow((const void*)mlp_up_kernel<true>) || !allow((const void*)mlp_down_kernel<false>) ||
+        !allow((const void*)mlp_down_kernel<true>))
       return XP_ERR_LAUNCH;
     g_lt_attr[dev] = true;
   }
@@ -1002,7 +1022,8 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
         !cached_map_bf16_2d(&mapWu, Wu, (uint64_t)H, (uint64_t)R, (uint64_t)H, 64, LT_BK))
       return XP_ERR_LAUNCH;
     void* args[] = {&mapUb, &mapWg, &mapWu, &p};
-    if (launch_ex((const void*)mlp_up_kernel, dim3((unsigned)(mtiles * p.htiles)), smem, stream, 1, args) !=
+    const void* up_fn = do_mlp ? (const void*)mlp_up_kernel<false> : (const void*)mlp_up_kernel<true>;
+    if (launch_ex(up_fn, dim3((unsigned)(mtiles * p.htiles)), smem, stream, 1, args) !=
         cudaSuccess)
       return XP_ERR_LAUNCH;
   }
@@ -1045,7 +1066,8 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
         !cached_map_plain_2d(&mapU, u, 4, (uint64_t)R, (uint64_t)rows, (uint64_t)R, (uint32_t)p.w, LT_BM))
       return XP_ERR_LAUNCH;
     void* args[] = {&mapM, &mapWd, &mapU, &p};
-    if (launch_ex((const void*)mlp_down_kernel, dim3((unsigned)(mtiles * p.ntiles * p.S)), smem, stream, p.S, args) !=
+    const void* down_fn = do_mlp ? (const void*)mlp_down_kernel<false> : (const void*)mlp_down_kernel<true>;
+    if (launch_ex(down_fn, dim3((unsigned)(mtiles * p.ntiles * p.S)), smem, stream, p.S, args) !=
         cudaSuccess)
       return XP_ERR_LAUNCH;
   }

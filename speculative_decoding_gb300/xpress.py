@@ -44,12 +44,17 @@ _SIGS = {
     "xp_latent_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _i64]),
     "xp_latent_pass": (ctypes.c_int32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                         _i64, _i64, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
+    "xp_latent_pass_ex": (ctypes.c_int32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                           _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int32, _vp, _sz, _vp]),
     "xp_readout_workspace_size": (_sz, [_i64, _i64]),
     "xp_readout_argmax": (ctypes.c_int32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _i64, _i64, _vp,
                                            _vp, _sz, _vp]),
     "xp_jacobi_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _i64, _i64]),
     "xp_jacobi_pass": (ctypes.c_int32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
                                         _i64, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
+    "xp_jacobi_pass_ex": (ctypes.c_int32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
+                                           _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int32, _vp, _vp, _sz,
+                                           _vp]),
     "xp_jacobi_fixpoint": (ctypes.c_int32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
                                             _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int32, _vp, _vp, _vp,
                                             _sz, _vp]),
@@ -156,17 +161,20 @@ def latent_workspace_size(N: int, B: int, D: int, R: int, H: int) -> int:
     return int(lib().xp_latent_workspace_size(N, B, D, R, H))
 
 
-def latent_pass(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, lat_out, ws, stream=None) -> None:
+def latent_pass(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, lat_out, ws, stream=None, do_mlp=True) -> None:
+    """The latent stage into lat_out [N, B-1, R].  ``do_mlp`` False selects the
+    GEMM schedule (bf16 g, v and residual; see xp_latent_pass_ex)."""
     N, B = blk.shape
     V, D = E.shape
     R = W_lat.shape[1]
     H = Wg.shape[1]
     bf = torch.bfloat16
-    _check(lib().xp_latent_pass(_ptr(blk, torch.int64, "blk"), _ptr(am1, torch.int64, "am1"),
-                                _ptr(hcache, bf, "hcache"), _ptr(E, bf, "E"), _ptr(W_lat, bf, "W_lat"),
-                                _ptr(L, torch.float32, "L"), _ptr(Wg, bf, "Wg"), _ptr(Wu, bf, "Wu"),
-                                _ptr(Wd, bf, "Wd"), _ptr(lat_out, bf, "lat_out"), N, B, V, D, R, H,
-                                _ptr(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream)))
+    _check(lib().xp_latent_pass_ex(_ptr(blk, torch.int64, "blk"), _ptr(am1, torch.int64, "am1"),
+                                   _ptr(hcache, bf, "hcache"), _ptr(E, bf, "E"), _ptr(W_lat, bf, "W_lat"),
+                                   _ptr(L, torch.float32, "L"), _ptr(Wg, bf, "Wg"), _ptr(Wu, bf, "Wu"),
+                                   _ptr(Wd, bf, "Wd"), _ptr(lat_out, bf, "lat_out"), N, B, V, D, R, H,
+                                   1 if do_mlp else 0, _ptr(ws, torch.uint8, "workspace"), ws.numel(),
+                                   _stream(stream)))
 
 
 def readout_workspace_size(rows: int, V: int) -> int:
@@ -189,20 +197,22 @@ def jacobi_workspace_size(N: int, B: int, V: int, D: int, R: int, H: int) -> int
     return int(lib().xp_jacobi_workspace_size(N, B, V, D, R, H))
 
 
-def jacobi_pass(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, W2t, base, ws, changed=None, stream=None) -> None:
-    """One pass in place on blk; W2t is the readout weight stored [V, R]."""
+def jacobi_pass(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, W2t, base, ws, changed=None, stream=None,
+                do_mlp=True) -> None:
+    """One pass in place on blk; W2t is the readout weight stored [V, R].
+    ``do_mlp`` as in latent_pass."""
     N, B = blk.shape
     V, D = E.shape
     R = W_lat.shape[1]
     H = Wg.shape[1]
     bf = torch.bfloat16
-    _check(lib().xp_jacobi_pass(_ptr(blk, torch.int64, "blk"), _ptr(am1, torch.int64, "am1"),
-                                _ptr(hcache, bf, "hcache"), _ptr(E, bf, "E"), _ptr(W_lat, bf, "W_lat"),
-                                _ptr(L, torch.float32, "L"), _ptr(Wg, bf, "Wg"), _ptr(Wu, bf, "Wu"),
-                                _ptr(Wd, bf, "Wd"), _ptr(W2t, bf, "W2t"), _ptr(base, bf, "base", False),
-                                _rowmajor(base, "base"), N, B, V, D, R, H,
-                                _ptr(changed, torch.int32, "changed"),
-                                _ptr(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream)))
+    _check(lib().xp_jacobi_pass_ex(_ptr(blk, torch.int64, "blk"), _ptr(am1, torch.int64, "am1"),
+                                   _ptr(hcache, bf, "hcache"), _ptr(E, bf, "E"), _ptr(W_lat, bf, "W_lat"),
+                                   _ptr(L, torch.float32, "L"), _ptr(Wg, bf, "Wg"), _ptr(Wu, bf, "Wu"),
+                                   _ptr(Wd, bf, "Wd"), _ptr(W2t, bf, "W2t"), _ptr(base, bf, "base", False),
+                                   _rowmajor(base, "base"), N, B, V, D, R, H, 1 if do_mlp else 0,
+                                   _ptr(changed, torch.int32, "changed"),
+                                   _ptr(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream)))
 
 
 def jacobi_fixpoint(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, W2t, base, ws, passes, max_passes=8,
