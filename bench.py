@@ -371,6 +371,20 @@ def run_gb300(args, rank, world, local_rank):
         if xpress.read_error(xws) != 0:
             raise RuntimeError("device-side error bits set in the multi-pass runs")
 
+        # ---- the same pass in the GEMM-MLP schedule (do_mlp = 0: bf16 g, v
+        # and residual), same inputs alternating
+        def gemm_step(i):
+            s = sets[i & 1]
+            xpress.jacobi_pass(s["blk"], s["am1"], s["hcache"], w["E"], w["W_lat"], L, w["Wg"], w["Wu"], w["Wd"],
+                               w["W2t"], s["base"], ws, do_mlp=False)
+
+        reset()
+        for i in range(max(3, args.warmup)):
+            gemm_step(i)
+        gm_us = events_time(stream, gemm_step, args.steps) / args.steps
+        if xpress.read_error(ws) != 0:
+            raise RuntimeError("device-side error bits set in the GEMM-MLP passes")
+
         # ---- end to end through the binding, host buffers, copies inside
         host = [dict(hcache=torch.from_numpy(src["hcache"].view(np.int16)).view(torch.bfloat16).pin_memory(),
                      base=torch.from_numpy(src["base"].view(np.int16)).view(torch.bfloat16).pin_memory(),
@@ -434,6 +448,7 @@ def run_gb300(args, rank, world, local_rank):
         "multipass": {"workload": "fixpoint N=64 B=16 V=152064 D=3584 R=512 H=1536, at most 8 passes",
                       "passes": fx_passes, "us_per_call": round(fx_us, 2),
                       "us_per_pass": round(fx_us / max(1, fx_passes), 2)},
+        "gemm_mlp": {"workload": sh.name + ", GEMM-MLP schedule (do_mlp = 0)", "us_per_pass": round(gm_us, 2)},
         "add_argmax": {"workload": "rows=480 V=152064 base+bias bf16", "us": round(aa_us, 2),
                        "GBps": round(aa_bytes / aa_us / 1e3, 1),
                        "frac": round(aa_bytes / aa_us / 1e3 / hbm_peak, 3), "peak": f"{peak_kind} {hbm_peak} GB/s",

@@ -483,16 +483,29 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   }
   __syncthreads();
   if (s_last) {
-    // every other CTA has folded its rows: publish the winners
+    // every other CTA has folded its rows (atomicMax, fence, then the done
+    // counter this CTA saw complete): read the winners with plain L2 loads,
+    // two rows per thread in flight together, publish them and zero the keys
+    // for the next call.  The old slot value is read only when a caller
+    // counts changes.
     __threadfence();
+    const bool count = p.changed != nullptr || p.passes_out != nullptr;
     int nchanged = 0;
-    for (int r = threadIdx.x; r < p.rows; r += blockDim.x) {
-      const unsigned long long k = atomicExch(&p.keys[r], 0ull);
+    auto publish = [&](int r, unsigned long long k) {
       const int64_t idx = (int64_t)key_index(k);
       const int64_t n = r / (p.B - 1), jj = r - n * (p.B - 1);
       int64_t* slot = p.blk + n * p.B + 1 + jj;
-      nchanged += (*slot != idx);
+      if (count) nchanged += (*slot != idx);
       *slot = idx;
+    };
+    for (int r0 = threadIdx.x; r0 < p.rows; r0 += 2 * blockDim.x) {
+      const int r1 = r0 + blockDim.x;
+      const unsigned long long k0 = __ldcg(&p.keys[r0]);
+      const unsigned long long k1 = r1 < p.rows ? __ldcg(&p.keys[r1]) : 0ull;
+      p.keys[r0] = 0ull;
+      if (r1 < p.rows) p.keys[r1] = 0ull;
+      publish(r0, k0);
+      if (r1 < p.rows) publish(r1, k1);
     }
     if (p.changed && nchanged) atomicAdd(p.changed, nchanged);
     // fixpoint driver: count the pass; a pass that changed no slot is the
