@@ -42,6 +42,8 @@ SHAPES = [
     synth.PassShape("t3", 5, 7, 3000, 200, 256, 192, 13),
     synth.PassShape("t4", 17, 16, 2048, 1024, 512, 512, 14),
     synth.PassShape("t5", 1, 2, 100, 64, 16, 64, 15),
+    # D = R: the pages' own layout (embedding already at the latent width)
+    synth.PassShape("dr", 6, 16, 3000, 512, 512, 256, 16),
 ]
 
 

@@ -60,7 +60,8 @@ def check_rows(orc, d, blk_in, blk_out, rows):
 
 
 SHAPES = [synth.TINY, synth.PassShape("p1", 9, 16, 3000, 256, 128, 256, 31),
-          synth.PassShape("p2", 4, 5, 1000, 128, 64, 128, 32)]
+          synth.PassShape("p2", 4, 5, 1000, 128, 64, 128, 32),
+          synth.PassShape("pdr", 5, 16, 2000, 256, 256, 256, 33)]  # D = R, the pages' layout
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=[s.name for s in SHAPES])
