@@ -405,26 +405,64 @@ def run_gb300(args, rank, world, local_rank):
             raise RuntimeError("device-side error bits set in the D = R passes")
         pp_shape = synth.PassShape("pp", N, B, V, R, R, H, 0)
 
-        # ---- end to end through the binding, host buffers, copies inside
+        # ---- end to end through the binding, host buffers, copies inside.
+        # Every step copies its inputs from pinned host memory and reads its
+        # result back; the copies run on their own streams (the large base
+        # split over several, so several copy engines share it), double
+        # buffered, so step i+1's inputs stream in while pass i runs.
         host = [dict(hcache=torch.from_numpy(src["hcache"].view(np.int16)).view(torch.bfloat16).pin_memory(),
                      base=torch.from_numpy(src["base"].view(np.int16)).view(torch.bfloat16).pin_memory(),
                      am1=torch.from_numpy(src["am1"]).pin_memory(), blk=torch.from_numpy(src["blk"]).pin_memory(),
                      out=torch.empty((N, B), dtype=torch.int64).pin_memory()) for src in (d, d2)]
-        dev_in = dict(hcache=torch.empty_like(sets[0]["hcache"]), base=torch.empty_like(sets[0]["base"]),
-                      am1=torch.empty_like(sets[0]["am1"]), blk=torch.empty_like(sets[0]["blk"]))
+        bufs = [dict(hcache=torch.empty_like(sets[0]["hcache"]), base=torch.empty_like(sets[0]["base"]),
+                     am1=torch.empty_like(sets[0]["am1"]), blk=torch.empty_like(sets[0]["blk"])) for _ in range(2)]
+        n_cs = 4
+        copy_streams = [torch.cuda.Stream(device) for _ in range(n_cs)]
+        landed = [[torch.cuda.Event() for _ in range(n_cs)] for _ in range(2)]
+        freed = [torch.cuda.Event() for _ in range(2)]
+        rows_per = (sh.rows + n_cs - 1) // n_cs
+
+        def issue_copy(i):
+            h, bf = host[i & 1], bufs[i & 1]
+            for c, cs in enumerate(copy_streams):
+                if i >= 2:
+                    cs.wait_event(freed[i & 1])  # the pass that last read this buffer is done
+                with torch.cuda.stream(cs):
+                    r0, r1 = c * rows_per, min(sh.rows, (c + 1) * rows_per)
+                    if r0 < r1:
+                        bf["base"][r0:r1].copy_(h["base"][r0:r1], non_blocking=True)
+                    if c == 0:
+                        for k in ("hcache", "am1", "blk"):
+                            bf[k].copy_(h[k], non_blocking=True)
+                landed[i & 1][c].record(cs)
 
         def e2e_step(i):
-            h = host[i & 1]
-            for k in ("hcache", "base", "am1", "blk"):
-                dev_in[k].copy_(h[k], non_blocking=True)
-            xpress.jacobi_pass(dev_in["blk"], dev_in["am1"], dev_in["hcache"], w["E"], w["W_lat"], L, w["Wg"],
-                               w["Wu"], w["Wd"], w["W2t"], dev_in["base"], ws)
-            h["out"].copy_(dev_in["blk"], non_blocking=True)
+            bf = bufs[i & 1]
+            for ev in landed[i & 1]:
+                stream.wait_event(ev)
+            xpress.jacobi_pass(bf["blk"], bf["am1"], bf["hcache"], w["E"], w["W_lat"], L, w["Wg"], w["Wu"],
+                               w["Wd"], w["W2t"], bf["base"], ws)
+            host[i & 1]["out"].copy_(bf["blk"], non_blocking=True)
+            freed[i & 1].record(stream)
+            issue_copy(i + 1)
 
-        for i in range(max(3, args.warmup)):
-            e2e_step(i)
-        torch.cuda.synchronize()
-        e2e_us = events_time(stream, e2e_step, args.steps) / args.steps
+        def e2e_run(steps):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for cs in copy_streams:
+                cs.wait_event(e0)
+            issue_copy(0)
+            for i in range(steps):
+                e2e_step(i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) * 1e3
+
+        e2e_run(max(3, args.warmup))
+        e2e_us = e2e_run(args.steps) / args.steps
+        if xpress.read_error(ws) != 0:
+            raise RuntimeError("device-side error bits set in the end-to-end passes")
         h2d = sum(host[0][k].numel() * host[0][k].element_size() for k in ("hcache", "base", "am1", "blk"))
         d2h = host[0]["out"].numel() * 8
 
