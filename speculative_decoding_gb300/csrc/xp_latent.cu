@@ -163,11 +163,10 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     // (the whole [B][B] square of L for these w channels)
     auto aux_copies = [&]() {
       aux_issued = true;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(aux_full, (uint32_t)(p.B * p.B * p.w * 4) + (uint32_t)(LT_BM * p.w * 2));
-        tma_load_2d(smem + p.hc_off, &mapHc, col0, mt * p.bpt * p.B, aux_full);
-        tma_load_2d(Ls, &mapL, col0, 0, aux_full);
-      }
+      if (lane == 0) mbar_arrive_expect_tx(aux_full, (uint32_t)(p.B * p.B * p.w * 4) + (uint32_t)(LT_BM * p.w * 2));
+      __syncwarp();
+      if (lane == 0) tma_load_2d(smem + p.hc_off, &mapHc, col0, mt * p.bpt * p.B, aux_full);
+      if (lane == 1) tma_load_2d(Ls, &mapL, col0, 0, aux_full);
       __syncwarp();
     };
     const uint64_t pol = policy_evict_last();  // every pass re-reads W_lat
@@ -518,8 +517,9 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
     }
     pdl_wait();
     if (lane == 0) XP_TRACE_MARK(18);
-    if (lane == 0)
-      for (int i = 0; i < pre; ++i) tma_load_2d(smem + (size_t)i * stage_bytes, &mapUb, i * LT_BK, mt * LT_BM, &full[i]);
+    // the first stages' ub boxes, one lane each (a single thread issues
+    // tiled copies one after another, ~0.27 us apiece)
+    if (lane < pre) tma_load_2d(smem + (size_t)lane * stage_bytes, &mapUb, lane * LT_BK, mt * LT_BM, &full[lane]);
     for (int i = pre; i < p.chunks; ++i) {
       const uint32_t s = i % p.stages, k = i / p.stages;
       int ok = 1;
@@ -711,9 +711,12 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
                          &full[i], pol);
     }
     pdl_wait();
-    if (lane == 0) {
-      XP_TRACE_MARK(34);
-      for (int i = 0; i < pre; ++i) tma_load_2d(smem + (size_t)i * stage_bytes, &mapM, (c0 + i) * LT_BK, mt * LT_BM, &full[i]);
+    if (lane == 0) XP_TRACE_MARK(34);
+    // the first stages' m boxes and the residual box, one lane each (a single
+    // thread issues tiled copies one after another, ~0.27 us apiece)
+    if (lane < pre)
+      tma_load_2d(smem + (size_t)lane * stage_bytes, &mapM, (c0 + lane) * LT_BK, mt * LT_BM, &full[lane]);
+    if (lane == 31) {
       mbar_arrive_expect_tx(aux_full, (uint32_t)(LT_BM * p.w * 4));
       tma_load_2d(smem + p.region, &mapU, col0, mt * LT_BM, aux_full);
     }
