@@ -187,6 +187,13 @@ def oracle_sample(d, shape, budget_s: float = 12.0):
 # reference arm: the CPU oracle
 # ---------------------------------------------------------------------------
 
+def workload_config(world: int) -> dict:
+    """The `config` object of both arms' JSON lines."""
+    return {"workload": SHAPE.name, "N": SHAPE.N, "B": SHAPE.B, "V": SHAPE.V, "D": SHAPE.D, "R": SHAPE.R,
+            "H": SHAPE.H, "parallelism": "replicas" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (W2 + base = 302 MB per pass; two sets of per-pass inputs alternate)"}
+
+
 def run_reference(args, world):
     d = synth.pass_inputs(SHAPE)
     oracle_sample(d, SHAPE, budget_s=0.0)  # warm-up: builds the oracle, one block and one row
@@ -202,8 +209,7 @@ def run_reference(args, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(value / 1e3, 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": SHAPE.name, "N": SHAPE.N, "B": SHAPE.B, "V": SHAPE.V, "D": SHAPE.D,
-                   "R": SHAPE.R, "H": SHAPE.H, "parallelism": "replicas"},
+        "config": workload_config(world),
         "cpu_baseline": {"value": round(value, 1), "unit": "us/pass", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 1), "unit": "us/pass", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -493,9 +499,7 @@ def run_gb300(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded; random weights of the stated shapes)",
-        "config": {"workload": sh.name, "N": N, "B": B, "V": V, "D": D, "R": R, "H": H,
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (W2 + base = 302 MB per pass; two sets of per-pass inputs alternate)"},
+        "config": workload_config(world),
         "pass": {"us": round(per_pass, 2), "passes_per_s": round(1e6 / per_pass, 1),
                  "rows_V_per_s": round(sh.rows * V / per_pass * 1e6, 1),
                  "roofline_us": round(max(pass_bytes(sh) / hbm_peak / 1e3, pass_flops(sh) / tf_peak / 1e6), 2),
