@@ -61,3 +61,34 @@ def test_read_error_validation(L):
     bits = ctypes.c_uint32()
     assert L.xp_read_error(None, None, ctypes.byref(bits)) == xpress.XP_ERR_NULL
     assert L.xp_read_error(FAKE + 1, None, ctypes.byref(bits)) == xpress.XP_ERR_WORKSPACE
+
+
+def _lp(L, do_mlp=0, N=2, B=4, V=1000, D=64, R=32, H=64, lat=FAKE, ws=FAKE, nbytes=1 << 24, ptr=FAKE):
+    return L.xp_latent_pass_ex(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, lat, N, B, V, D, R, H, do_mlp, ws,
+                               nbytes, None)
+
+
+def _jp(L, do_mlp=0, N=2, B=4, V=1000, D=64, R=32, H=64, ld=1000, ws=FAKE, nbytes=1 << 24, ptr=FAKE):
+    return L.xp_jacobi_pass_ex(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ld, N, B, V, D, R, H, do_mlp,
+                               None, ws, nbytes, None)
+
+
+def test_schedule_entry_points_host_validation(L):
+    """The do_mlp entry points reject bad arguments before any CUDA call.
+    (No call here passes every check: on a GPU machine that would launch
+    kernels on the dummy addresses.)"""
+    for f in (_lp, _jp):
+        assert f(L, do_mlp=2) == xpress.XP_ERR_SHAPE
+        assert f(L, do_mlp=-1) == xpress.XP_ERR_SHAPE
+        assert f(L, B=1) == xpress.XP_ERR_SHAPE
+        assert f(L, B=17) == xpress.XP_ERR_SHAPE
+        assert f(L, R=24) == xpress.XP_ERR_ALIGN        # R a multiple of 16
+        assert f(L, H=96) == xpress.XP_ERR_ALIGN        # H a multiple of 64
+        assert f(L, ptr=0) == xpress.XP_ERR_NULL
+        assert f(L, ws=FAKE + 16) == xpress.XP_ERR_WORKSPACE
+        assert f(L, nbytes=64) == xpress.XP_ERR_WORKSPACE
+    assert _lp(L, lat=0) == xpress.XP_ERR_NULL
+    assert _lp(L, lat=FAKE + 8) == xpress.XP_ERR_ALIGN
+    assert _jp(L, ld=999) == xpress.XP_ERR_SHAPE        # ld_base < V
+    assert _jp(L, ld=1004) == xpress.XP_ERR_ALIGN       # ld_base a multiple of 8
+    assert _lp(L, N=0) == xpress.XP_OK                  # empty: no-op
