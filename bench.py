@@ -368,6 +368,14 @@ def run_gb300(args, rank, world, local_rank):
         torch.cuda.synchronize()
         floor_reps = 10000
         floor_us = events_time(stream, lambda i: graph.replay(), floor_reps) / floor_reps
+        # the median of single replays, each between its own pair of events
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(1000)]
+        for e0, e1 in ev:
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        floor_med = float(np.median([e0.elapsed_time(e1) * 1e3 for e0, e1 in ev]))
         if xpress.read_error(fws) != 0:
             raise RuntimeError("device-side error bits set in the latency-floor replays")
 
@@ -517,7 +525,8 @@ def run_gb300(args, rank, world, local_rank):
                  "frac_of_roofline": round(max(pass_bytes(sh) / hbm_peak / 1e3,
                                                pass_flops(sh) / tf_peak / 1e6) / per_pass, 3)},
         "latency_floor": {"workload": "pass N=1 B=16 V=152064 D=3584 R=512 H=1536, CUDA graph replay",
-                          "replays": floor_reps, "us_per_pass": round(floor_us, 2)},
+                          "replays": floor_reps, "us_per_pass": round(floor_us, 2),
+                          "median_us_single_replay": round(floor_med, 2)},
         "multipass": {"workload": "fixpoint N=64 B=16 V=152064 D=3584 R=512 H=1536, at most 8 passes",
                       "passes": fx_passes, "us_per_call": round(fx_us, 2),
                       "us_per_pass": round(fx_us / max(1, fx_passes), 2)},
