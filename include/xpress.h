@@ -270,6 +270,19 @@ XP_API xp_status xp_jacobi_fixpoint(int64_t* d_blk, const int64_t* d_am1, const 
                                     size_t workspace_bytes, xp_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * xp_selftest_wait_timeout -- failure-detection self-test.  Enqueues one
+ * small kernel that runs the library's bounded mbarrier wait on a barrier
+ * nothing arrives on, with a limit of limit_us microseconds (1 .. 2,000,000)
+ * instead of the kernels' 2 s.  The wait gives up, the kernel sets
+ * XP_DEVERR_TIMEOUT in the workspace header and returns: xp_read_error()
+ * then reports the bit, and the context stays usable.  No copy is in flight
+ * and no memory besides the header is touched.  d_workspace: any workspace
+ * of at least 256 bytes (256-byte aligned).
+ * ---------------------------------------------------------------------- */
+XP_API xp_status xp_selftest_wait_timeout(void* d_workspace, size_t workspace_bytes, uint32_t limit_us,
+                                          xp_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * xp_read_error -- copy the workspace's device-side error bits (XP_DEVERR_*)
  * to *host_bits and clear them.  Synchronises `stream`; do not call it while
  * the stream is being captured into a CUDA graph.

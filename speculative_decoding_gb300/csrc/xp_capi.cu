@@ -247,6 +247,16 @@ xp_status xp_jacobi_fixpoint(int64_t* d_blk, const int64_t* d_am1, const xp_bf16
   return XP_OK;
 }
 
+xp_status xp_selftest_wait_timeout(void* d_workspace, size_t workspace_bytes, uint32_t limit_us,
+                                   xp_stream_t stream) {
+  if (!d_workspace) return XP_ERR_NULL;
+  if (!aligned256(d_workspace) || workspace_bytes < sizeof(xp::WsHeader)) return XP_ERR_WORKSPACE;
+  if (limit_us < 1 || limit_us > 2000000u) return XP_ERR_SHAPE;
+  xp_status st = check_device();
+  if (st != XP_OK) return st;
+  return xp::launch_wait_timeout_probe(d_workspace, 1000ull * limit_us, (cudaStream_t)stream);
+}
+
 xp_status xp_read_error(void* d_workspace, xp_stream_t stream, uint32_t* host_bits) {
   if (!d_workspace || !host_bits) return XP_ERR_NULL;
   if (!aligned256(d_workspace)) return XP_ERR_WORKSPACE;

@@ -34,4 +34,7 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
                         int64_t H, void* ws, cudaStream_t stream, const uint32_t* skip = nullptr,
                         bool do_mlp = true);
 
+// The failure-detection self-test: a bounded wait that runs out (limit_ns).
+xp_status launch_wait_timeout_probe(void* ws, unsigned long long limit_ns, cudaStream_t stream);
+
 }  // namespace xp

@@ -59,6 +59,7 @@ _SIGS = {
                                             _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int32, _vp, _vp, _vp,
                                             _sz, _vp]),
     "xp_read_error": (ctypes.c_int32, [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]),
+    "xp_selftest_wait_timeout": (ctypes.c_int32, [_vp, _sz, ctypes.c_uint32, _vp]),
 }
 
 
@@ -237,3 +238,10 @@ def read_error(ws, stream=None) -> int:
     bits = ctypes.c_uint32(0)
     _check(lib().xp_read_error(_ptr(ws, torch.uint8, "workspace"), _stream(stream), ctypes.byref(bits)))
     return int(bits.value)
+
+
+def selftest_wait_timeout(ws, limit_us: int = 1000, stream=None) -> None:
+    """Enqueue the failure-detection self-test: a bounded device wait that runs
+    out after limit_us and sets XP_DEVERR_TIMEOUT (read it with read_error)."""
+    _check(lib().xp_selftest_wait_timeout(_ptr(ws, torch.uint8, "workspace"), ws.numel(), limit_us,
+                                          _stream(stream)))
