@@ -315,10 +315,6 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
         }
         tc_fence_after();
         if (t == 0) XP_TRACE_MARK(3);
-#ifdef XP_TRACE
-        if (t == 0 || t == ntiles - 1) g_trace[blockIdx.x * kTraceSlots + 58 + (t != 0)] = clock64();
-        if (t == ntiles - 1) XP_TRACE_MARK(60);
-#endif
         if (t < 16) XP_TRACE_MARK(26 + t);
         const uint32_t d = tmem + RO_TMEM_ACC + a * RO_BN;
         // A: TMEM columns hold K pairs; a K step of 16 is 8 columns.
