@@ -91,7 +91,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
                 const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUtensorMap mapU,
                 const __grid_constant__ CUtensorMap mapUb, const ProjParams p) {
   extern __shared__ uint8_t smem_raw[];
-  if (pass_skipped(p.skip)) return;
+  if (pass_skipped(p.skip, true)) return;  // the first kernel of a pass
   if (threadIdx.x == 0) XP_TRACE_MARK(0);
   if (threadIdx.x == 0) XP_TRACE_SM(15);
   uint8_t* smem = align1024(smem_raw);
@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(LT_THREADS, 1)
 mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__ CUtensorMap mapWg,
               const __grid_constant__ CUtensorMap mapWu, const UpParams p) {
   extern __shared__ uint8_t smem_raw[];
-  if (pass_skipped(p.skip)) return;
+  if (pass_skipped(p.skip, false)) return;
   if (threadIdx.x == 0) XP_TRACE_MARK(16);
   uint8_t* smem = align1024(smem_raw);
   constexpr uint32_t stage_bytes = LT_A_CHUNK + 2 * LT_BOX;  // 32 KB
@@ -644,7 +644,7 @@ __global__ void __launch_bounds__(LT_THREADS, 2)
 mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant__ CUtensorMap mapWd,
                 const __grid_constant__ CUtensorMap mapU, const DownParams p) {
   extern __shared__ uint8_t smem_raw[];
-  if (pass_skipped(p.skip)) return;
+  if (pass_skipped(p.skip, false)) return;
   if (threadIdx.x == 0) XP_TRACE_MARK(32);
   uint8_t* smem = align1024(smem_raw);
   const uint32_t b_bytes = (uint32_t)p.tn * LT_BK * 2;

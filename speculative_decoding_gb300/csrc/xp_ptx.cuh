@@ -370,15 +370,19 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 // Multi-pass launches of a fixed count: every kernel of a pass launched after
 // the fixpoint was reached exits at once.  `skip` (nullable) is the flag the
-// last pass's readout set; thread 0 reads it after the dependency wait (the
-// preceding kernels, and through them the pass that set it, are complete),
-// and the CTA agrees on it.  Returns true when this CTA must exit.
-__device__ __forceinline__ bool pass_skipped(const uint32_t* skip) {
+// last pass's readout set; thread 0 reads it and the CTA agrees on it.
+// Returns true when this CTA must exit.  The pass's first kernel reads it
+// after its dependency wait (wait_first: the previous pass, which sets the
+// flag, is then complete).  The later kernels of a pass read it at once:
+// they are launched only after every CTA of the first kernel has passed
+// that wait, so the flag is final by then, and their prologues keep
+// overlapping the kernel before them.
+__device__ __forceinline__ bool pass_skipped(const uint32_t* skip, bool wait_first) {
   __shared__ uint32_t s_skip;
   if (skip == nullptr) return false;
   if (threadIdx.x == 0) {
-    pdl_wait();
-    s_skip = *reinterpret_cast<const volatile uint32_t*>(skip);
+    if (wait_first) pdl_wait();
+    s_skip = ld_acquire_gpu(skip);  // from L2, never a stale L1 line
   }
   __syncthreads();
   return s_skip != 0u;

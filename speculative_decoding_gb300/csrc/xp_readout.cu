@@ -133,7 +133,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   uint64_t* a_free = a_full + 2;  // the epilogue warps copied a round to TMEM
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(a_free + 1);
   __shared__ int s_last;
-  if (pass_skipped(p.skip)) return;  // both CTAs of a pair read the same flag
+  if (pass_skipped(p.skip, false)) return;  // both CTAs of a pair read the same flag
   if (threadIdx.x == 0) XP_TRACE_MARK(0);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
