@@ -33,8 +33,9 @@
 //     (two 128-column TMEM accumulators: the epilogue of tile t overlaps the
 //     MMAs of tile t+1) and commits them ONCE per tile to the barriers of
 //     both CTAs: that commit both hands the accumulator to the epilogue and
-//     frees the W2 slot of tile t for tile t+2 (a pair's commit is costly, so
-//     there is no separate per-stage release);
+//     frees the W2 slot of tile t for tile t+2 (each CTA's W2 half-tile is
+//     one contiguous 64 KB block of W2t; loading and releasing it in K parts
+//     was slower);
 //   * warps 2..9 drain the accumulator with tcgen05.ld (thread = one row,
 //     warp = a 32-lane quadrant and a 64-column half), round to bf16, add the
 //     base tile from shared memory and keep a running (max, first column)
