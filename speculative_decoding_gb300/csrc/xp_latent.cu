@@ -541,7 +541,11 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(LT_BM, 64, 0, 1);
+      // one N=128 MMA per K step computes [g | v]: the stage's Wg and Wu
+      // boxes sit one box apart, which is the B descriptor's stride between
+      // its two 64-wide N chunks, and TMEM columns [0, 64) / [64, 128) take
+      // g / v (an N=64 MMA runs at ~64 % of the N=128 rate)
+      constexpr uint32_t idesc = idesc_bf16_f32(LT_BM, 128, 0, 1);
       bool dead = false;
       for (int i = 0; i < p.chunks; ++i) {
         const uint32_t s = i % p.stages, k = i / p.stages;
@@ -555,10 +559,8 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
 #pragma unroll
         for (int kk = 0; kk < LT_BK / 16; ++kk) {
           const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
-          const uint64_t gdesc = smem_desc_sw128(a_base + LT_A_CHUNK + kk * 2048, LT_BOX, 1024);
-          const uint64_t vdesc = smem_desc_sw128(a_base + LT_A_CHUNK + LT_BOX + kk * 2048, LT_BOX, 1024);
-          tc_mma_f16(tmem, adesc, gdesc, idesc, (i | kk) != 0);
-          tc_mma_f16(tmem + 64, adesc, vdesc, idesc, (i | kk) != 0);
+          const uint64_t gvdesc = smem_desc_sw128(a_base + LT_A_CHUNK + kk * 2048, LT_BOX, 1024);
+          tc_mma_f16(tmem, adesc, gvdesc, idesc, (i | kk) != 0);
         }
         tc_commit(&empty[s]);
       }
