@@ -172,11 +172,5 @@ __host__ inline LatentWsLayout latent_ws_layout(int64_t N, int64_t B, int64_t D,
 
 __device__ __forceinline__ void flag_error(WsHeader* h, unsigned int bits) { atomicOr(&h->err, bits); }
 
-// a bounded wait gave up at `site`: set the timeout bit and remember the
-// first site
-__device__ __forceinline__ void flag_timeout(WsHeader* h, unsigned int site) {
-  atomicOr(&h->err, XP_DEVERR_TIMEOUT);
-  atomicCAS(&h->where, 0u, site);
-}
 
 }  // namespace xp

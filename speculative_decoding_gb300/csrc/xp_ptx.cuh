@@ -180,14 +180,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   return r;
 }
 
-// load a float from the shared memory of CTA `rank` of the cluster, at the
-// offset of `local` in this CTA
-__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
-  const uint32_t a = mapa_shared(smem_u32(local), rank);
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-  return v;
-}
 
 // load 16 bytes from the shared memory of CTA `rank` of the cluster, at the
 // offset of `local` (16-byte aligned) in this CTA
@@ -212,11 +204,6 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthread
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void cp_async_16(void* dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-// 4-byte form (bytes past src_bytes, 0 or 4, are zero-filled)
-__device__ __forceinline__ void cp_async_4(void* dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
                : "memory");
 }
 // wait until every cp.async this thread issued has landed in shared memory
@@ -249,21 +236,7 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 
 // close the group of this thread's cp.async issued since the last commit
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// wait until at most N of this thread's committed groups are still in flight
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
-// L2 prefetch of the 128-byte line holding `p`, kept with evict-last priority
-__device__ __forceinline__ void prefetch_l2_last(const void* p) {
-  asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
-}
-// L2 prefetch of `bytes` (a multiple of 16) contiguous bytes from a 16-byte
-// aligned address, by the bulk-copy engine (no shared memory involved)
-__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 // L2 prefetch of one tensor-map box (no shared memory involved)
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
@@ -301,14 +274,6 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 // wait until this thread's committed bulk stores are complete (written)
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// 1-D bulk copy global -> this CTA's shared memory (both addresses 16-byte
-// aligned, bytes a multiple of 16), completing on `bar` by transaction count
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
 
 // ---------------------------------------------------------------------------
 // CTA pairs (a cluster of two CTAs issuing tcgen05 with .cta_group::2): the
@@ -423,16 +388,6 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]: A read from tensor memory (lane = row,
-// each 32-bit column holds two consecutive K elements).
-__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                              uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 
 // Arrive (once) on an mbarrier when all previously issued tcgen05.mma of
 // this thread have completed.
