@@ -80,7 +80,7 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
 struct WsHeader {
   unsigned int err;         // XP_DEVERR_* bits
   unsigned int done;        // CTAs of the current readout grid that finished
-  unsigned int where;       // site code of the first wait that gave up (diagnostics)
+  unsigned int where;       // reserved (zero)
   // xp_jacobi_fixpoint: nonzero once a pass changed no slot (the passes
   // launched after it exit at once), and the number of passes that ran
   unsigned int converged;
