@@ -69,12 +69,15 @@ def readout_flops(shape) -> float:
 
 def pass_bytes(shape) -> int:
     """Algorithmic bytes of one pass: every weight and input read once (only
-    the embedding rows the tokens touch), the latent written and read once."""
+    the embedding rows the tokens touch), the latent written and read once,
+    the new tokens written."""
     N, B, V, D, R, H = shape.N, shape.B, shape.V, shape.D, shape.R, shape.H
-    w = D * R + 2 * R * H + H * R + R * V
-    inputs = N * B * D + N * B * R + N * (B - 1) * V + B * B * R * 2 + N * B * 8 + N * 8
-    lat = 2 * N * (B - 1) * R
-    return 2 * (w + inputs) + lat + N * (B - 1) * 8
+    bf16 = (D * R + 2 * R * H + H * R + R * V      # W_lat, Wg, Wu, Wd, W2
+            + N * B * D + N * B * R + N * (B - 1) * V)  # gathered E rows, hcache, base
+    mixer = 4 * B * B * R                           # L, fp32
+    tokens_in = 8 * (N * B + N)                     # blk, am1
+    lat = 2 * (2 * N * (B - 1) * R)                 # bf16 latent: written, then read
+    return 2 * bf16 + mixer + tokens_in + lat + 8 * N * (B - 1)
 
 
 def pass_flops(shape) -> float:

@@ -37,3 +37,21 @@ def test_reference_arm_line(monkeypatch):
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "us/pass", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_roofline_arithmetic():
+    """The algorithmic counts the roofline fractions divide by, for the pass
+    workload (N=32, B=16, V=152064, D=3584, R=512, H=1536): the readout reads
+    W2 (R*V*2), base (rows*V*2) and the latent (rows*R*2) once; the pass adds
+    the latent stage's weights and inputs and the latent's write."""
+    import bench
+    from speculative_decoding_gb300 import synth
+
+    sh = synth.SERVE
+    assert sh.rows == 480
+    assert bench.readout_bytes(sh) == 155_713_536 + 145_981_440 + 491_520 == 302_186_496
+    assert bench.readout_flops(sh) == 2.0 * 480 * 152064 * 512
+    assert abs(bench.pass_bytes(sh) / 1e6 - 315.8) < 0.1
+    assert abs(bench.pass_flops(sh) / 1e9 - 78.89) < 0.01
+    # at the measured 6790.7 GB/s the pass is HBM-bound at 46.5 us
+    assert abs(bench.pass_bytes(sh) / 6790.7 / 1e3 - 46.5) < 0.05
