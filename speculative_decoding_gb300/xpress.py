@@ -2,8 +2,10 @@
 
 Every function takes torch CUDA tensors, checks dtype/device/contiguity, and
 passes raw device pointers plus the current CUDA stream to the C entry point of
-the same name (see include/xpress.h for the contracts).  Nothing here computes:
-if the library is missing, ``lib()`` raises -- there is no fallback.
+the same name (``latent_pass`` and ``jacobi_pass`` call the ``_ex`` forms, which
+also take the MLP schedule; see include/xpress.h for the contracts).  Nothing
+here computes: if the library is missing, ``lib()`` raises -- there is no
+fallback.
 """
 
 from __future__ import annotations
