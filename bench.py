@@ -50,6 +50,11 @@ PROFILE = os.path.join(ROOT, "profiles", "readout_argmax_N32_B16_V152064.md")
 READOUT_SRC = os.path.join(ROOT, "speculative_decoding_gb300", "csrc", "xp_readout.cu")
 
 
+# nominal figures of the part (context beside the measured denominators)
+NOMINAL_HBM_GBS = 8000.0
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
 def peaks():
     if os.path.exists(PEAKS):
         with open(PEAKS) as f:
@@ -498,7 +503,27 @@ def run_gb300(args, rank, world, local_rank):
         h2d = sum(host[0][k].numel() * host[0][k].element_size() for k in ("hcache", "base", "am1", "blk"))
         d2h = host[0]["out"].numel() * 8
 
-    us, ro_us, aa_us, e2e_us = max_over_ranks([us, ro_us, aa_us, e2e_us], world, device)
+        # the host link alone: the same copies (same four streams, same split)
+        # with no pass between them, back to back
+        def link_run(steps):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for cs in copy_streams:
+                cs.wait_event(e0)
+            for i in range(steps):
+                issue_copy(i)
+                for ev in landed[i & 1]:
+                    stream.wait_event(ev)
+                freed[i & 1].record(stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) * 1e3
+
+        link_run(3)
+        link_us = link_run(args.steps) / args.steps
+
+    us, ro_us, aa_us, e2e_us, link_us = max_over_ranks([us, ro_us, aa_us, e2e_us, link_us], world, device)
     if rank != 0:
         return
     per_pass = whole_job_per_pass(us, args.steps, world)
@@ -526,7 +551,9 @@ def run_gb300(args, rank, world, local_rank):
                  "rows_V_per_s": round(sh.rows * V / per_pass * 1e6, 1),
                  "roofline_us": round(max(pass_bytes(sh) / hbm_peak / 1e3, pass_flops(sh) / tf_peak / 1e6), 2),
                  "frac_of_roofline": round(max(pass_bytes(sh) / hbm_peak / 1e3,
-                                               pass_flops(sh) / tf_peak / 1e6) / per_pass, 3)},
+                                               pass_flops(sh) / tf_peak / 1e6) / per_pass, 3),
+                 "frac_of_nominal_roofline": round(max(pass_bytes(sh) / NOMINAL_HBM_GBS / 1e3,
+                                                       pass_flops(sh) / NOMINAL_BF16_TFLOPS / 1e6) / per_pass, 3)},
         "latency_floor": {"workload": "pass N=1 B=16 V=152064 D=3584 R=512 H=1536, CUDA graph replay",
                           "replays": floor_reps, "us_per_pass": round(floor_us, 2),
                           "median_us_single_replay": round(floor_med, 2)},
@@ -541,15 +568,20 @@ def run_gb300(args, rank, world, local_rank):
         "add_argmax": {"workload": "rows=480 V=152064 base+bias bf16", "us": round(aa_us, 2),
                        "GBps": round(aa_bytes / aa_us / 1e3, 1),
                        "frac": round(aa_bytes / aa_us / 1e3 / hbm_peak, 3), "peak": f"{peak_kind} {hbm_peak} GB/s",
+                       "frac_of_nominal": round(aa_bytes / aa_us / 1e3 / NOMINAL_HBM_GBS, 3),
                        "rows_V_per_s": round(synth.ARGMAX_ROWS * synth.ARGMAX_V / aa_us * 1e6, 1)},
         "roofline": {"kernel": "readout_argmax_kernel", "bound": "hbm", "achieved": round(ro_achieved, 1),
                      "peak": hbm_peak, "unit": "GB/s", "frac": round(ro_achieved / hbm_peak, 3),
                      "traffic": traffic_from_profile(), "us_per_launch": round(ro_us, 2),
                      "algorithmic_bytes": readout_bytes(sh),
-                     "tflops": round(readout_flops(sh) / ro_us / 1e6, 1), "peak_kind": peak_kind},
+                     "tflops": round(readout_flops(sh) / ro_us / 1e6, 1), "peak_kind": peak_kind,
+                     "frac_of_nominal": round(ro_achieved / NOMINAL_HBM_GBS, 3)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_per_pass, 2), "unit": "us/pass", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
+                "d2h_bytes_per_step": int(d2h),
+                "link": {"what": "the same pinned host-to-device copies alone, back to back (four streams)",
+                         "us_per_step": round(link_us, 2), "GBps": round(h2d / link_us / 1e3, 1),
+                         "e2e_frac_of_link": round(link_us / (e2e_us), 3)}},
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }

@@ -18,8 +18,13 @@
  *   enqueues work on `stream` (0 = the legacy default stream).
  * - bf16 data is passed as xp_bf16 (the 16-bit pattern of a bfloat16).  Tokens
  *   are int64.  The mixer L is float32.
- * - Matrices are row-major; weights are stored [in, out] ("transposed" as on
- *   the pages: W_lat [D,R], Wg/Wu [R,H], Wd [H,R], W2 [R,V]).
+ * - Matrices are row-major; the latent-stage weights are stored [in, out]
+ *   ("transposed" as on the pages: W_lat [D,R], Wg/Wu [R,H], Wd [H,R]).
+ *   The readout weight is the one exception: the pages multiply by W2 [R,V],
+ *   but every entry point here takes it vocabulary-major, as W2t = W2
+ *   transposed, [V,R] (parameter d_W2t), so that the weights of one vocab
+ *   tile are one contiguous block.  Passing W2 [R,V] itself is NOT detected
+ *   (a raw pointer carries no shape) and gives wrong tokens.
  * - Alignment: every bf16 pointer must be 16-byte aligned and every leading
  *   dimension (ld_*) a multiple of 8 elements, else XP_ERR_ALIGN.  Sizes are
  *   otherwise free (V need not be a multiple of 8 for xp_add_argmax).
@@ -112,8 +117,11 @@ XP_API xp_status xp_add_argmax(const xp_bf16* d_base, int64_t ld_base, const xp_
  *
  * The first call on each device (with that device current) looks up the
  * scratch's device address, which may load the library's device code; make
- * that first call before any stream capture.  Later calls only read the
- * cached address.
+ * that first call before any stream capture.  The address belongs to the
+ * CUDA context it was looked up in: the cache is keyed by device and context
+ * id, so after a device reset, or with another context of the device made
+ * current, the next call looks it up again (that call is again a first call,
+ * to be made outside capture).  Other calls only read the cached address.
  *
  * There is one scratch per device: calls that can overlap in time (on
  * different streams without ordering between them, or from several host
@@ -202,9 +210,9 @@ XP_API xp_status xp_latent_pass_ex(const int64_t* d_blk, const int64_t* d_am1, c
  *   s[r,v]    = bf16(float(base[r*ld_base+v]) + float(bias[r,v]))
  *   blk[n*B + 1 + j] = lowest argmax_v s[r,v]               r = n*(B-1)+j
  *
- * d_lat [rows,R] bf16 dense.  d_W2t [V,R] bf16 dense: the readout weight W2
- * stored vocabulary-major (W2 transposed; the layout of a linear layer's
- * weight), so one vocab tile's weights are contiguous.  d_base [rows,V] with
+ * d_lat [rows,R] bf16 dense.  d_W2t: [V,R] bf16 dense -- the readout weight
+ * W2 [R,V] of the pages stored TRANSPOSED (vocabulary-major; the layout of a
+ * linear layer's weight), so one vocab tile's weights are contiguous.  d_base [rows,V] with
  * row stride ld_base.  R a multiple of 8 in [8, 512].  d_changed (nullable,
  * device int32): incremented by the number of slots whose token differs from
  * the value blk held before the call.  Workspace:
@@ -221,26 +229,27 @@ XP_API xp_status xp_readout_argmax(const xp_bf16* d_lat, const xp_bf16* d_W2t, c
  * its output (kept in the workspace), writing blk[:,1:] in place.  Repeated
  * calls iterate the Jacobi fixpoint: each pass reads the blk written by the
  * previous one (_xpress_add_argmax_reduce_to_blk_kernel docstring).
- * d_W2t [V,R] is the readout weight stored vocabulary-major, as in
- * xp_readout_argmax.  d_changed as in xp_readout_argmax.  Constraints: those
- * of both stages.
+ * d_W2t: [V,R] bf16 dense -- the readout weight W2 [R,V] of the pages stored
+ * TRANSPOSED (vocabulary-major), as in xp_readout_argmax.  d_changed as in
+ * xp_readout_argmax.  Constraints: those of both stages.
  * Workspace: xp_jacobi_workspace_size(N,B,V,D,R,H).
  * ---------------------------------------------------------------------- */
 XP_API size_t xp_jacobi_workspace_size(int64_t N, int64_t B, int64_t V, int64_t D, int64_t R, int64_t H);
 XP_API xp_status xp_jacobi_pass(int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_hcache,
                          const xp_bf16* d_E, const xp_bf16* d_W_lat, const float* d_L,
                          const xp_bf16* d_Wg, const xp_bf16* d_Wu, const xp_bf16* d_Wd,
-                         const xp_bf16* d_W2, const xp_bf16* d_base, int64_t ld_base, int64_t N,
+                         const xp_bf16* d_W2t, const xp_bf16* d_base, int64_t ld_base, int64_t N,
                          int64_t B, int64_t V, int64_t D, int64_t R, int64_t H,
                          int32_t* d_changed, void* d_workspace, size_t workspace_bytes,
                          xp_stream_t stream);
 
 /* xp_jacobi_pass_ex -- xp_jacobi_pass with the latent stage's MLP schedule
- * selectable: do_mlp as in xp_latent_pass_ex (1 = xp_jacobi_pass). */
+ * selectable: do_mlp as in xp_latent_pass_ex (1 = xp_jacobi_pass).
+ * d_W2t: [V,R], the readout weight transposed, as in xp_jacobi_pass. */
 XP_API xp_status xp_jacobi_pass_ex(int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_hcache,
                                    const xp_bf16* d_E, const xp_bf16* d_W_lat, const float* d_L,
                                    const xp_bf16* d_Wg, const xp_bf16* d_Wu, const xp_bf16* d_Wd,
-                                   const xp_bf16* d_W2, const xp_bf16* d_base, int64_t ld_base, int64_t N,
+                                   const xp_bf16* d_W2t, const xp_bf16* d_base, int64_t ld_base, int64_t N,
                                    int64_t B, int64_t V, int64_t D, int64_t R, int64_t H, int32_t do_mlp,
                                    int32_t* d_changed, void* d_workspace, size_t workspace_bytes,
                                    xp_stream_t stream);
@@ -256,6 +265,7 @@ XP_API xp_status xp_jacobi_pass_ex(int64_t* d_blk, const int64_t* d_am1, const x
  * small memsets), so the call is a fixed sequence of stream work (capturable
  * in a CUDA graph); the kernels of a pass enqueued after the fixpoint find the
  * workspace's convergence flag set and exit at their first instruction.
+ * d_W2t: [V,R], the readout weight transposed, as in xp_jacobi_pass.
  * d_passes (device int32, required) receives the number of passes that ran;
  * d_changed (nullable, device int32) is incremented by the slots each pass
  * changed.  max_passes in [1, 1024].  Other arguments, constraints and the
@@ -264,7 +274,7 @@ XP_API xp_status xp_jacobi_pass_ex(int64_t* d_blk, const int64_t* d_am1, const x
 XP_API xp_status xp_jacobi_fixpoint(int64_t* d_blk, const int64_t* d_am1, const xp_bf16* d_hcache,
                                     const xp_bf16* d_E, const xp_bf16* d_W_lat, const float* d_L,
                                     const xp_bf16* d_Wg, const xp_bf16* d_Wu, const xp_bf16* d_Wd,
-                                    const xp_bf16* d_W2, const xp_bf16* d_base, int64_t ld_base, int64_t N,
+                                    const xp_bf16* d_W2t, const xp_bf16* d_base, int64_t ld_base, int64_t N,
                                     int64_t B, int64_t V, int64_t D, int64_t R, int64_t H, int32_t max_passes,
                                     int32_t* d_passes, int32_t* d_changed, void* d_workspace,
                                     size_t workspace_bytes, xp_stream_t stream);

@@ -15,7 +15,9 @@
 // last CTA of a row (arrival counter) writes blk and re-zeroes the key and
 // counter, so the workspace is clean for the next call and no second launch
 // or partial buffer is needed.
-#include <atomic>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "xp_common.cuh"
@@ -142,36 +144,73 @@ xp_status launch_add_argmax(const uint16_t* base, int64_t ld_base, const uint16_
 // ---------------------------------------------------------------------------
 // Allocation-free variant: the keys and counters live in one fixed array of
 // device memory per device instead of a caller workspace.  Its layout is the
-// workspace layout of argmax_ws() for up to XP_ADD_ARGMAX_NOALLOC_MAX_ROWS rows.
+// workspace layout of argmax_ws() for up to XP_ADD_ARGMAX_NOALLOC_MAX_ROWS rows
+// (the size is taken from argmax_ws_bytes itself, so the two cannot drift).
 // ---------------------------------------------------------------------------
-constexpr size_t kNoallocBytes = 256 + ((8 * (size_t)XP_ADD_ARGMAX_NOALLOC_MAX_ROWS + 255) & ~size_t(255)) +
-                                 ((4 * (size_t)XP_ADD_ARGMAX_NOALLOC_MAX_ROWS + 255) & ~size_t(255));
+constexpr size_t kNoallocBytes = argmax_ws_bytes(XP_ADD_ARGMAX_NOALLOC_MAX_ROWS);
 static __device__ __align__(256) unsigned char g_add_argmax_scratch[kNoallocBytes];
 
 namespace {
 constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_ptr[kMaxDevices];
+
+// The scratch's device address belongs to the CUDA context that loaded this
+// module: a device reset, or a caller that makes another context of the same
+// device current, gives a different address.  So the cached address is kept
+// with the id of the context it was looked up in (cuCtxGetId: unique for the
+// life of the process) and looked up again when the current context differs.
+struct ScratchEntry {
+  unsigned long long ctx_id = 0;  // 0: nothing cached
+  void* ptr = nullptr;
+};
+ScratchEntry g_scratch[kMaxDevices];
 std::mutex g_scratch_mu;
 
-// Device address of this device's scratch; looked up once per device with
-// that device current (the lookup may load this module's device code).
+// id of the current context, through the runtime's driver entry points (the
+// library does not link libcuda); 0 when it cannot be read
+unsigned long long current_ctx_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+  });
+  if (!get_cur || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_cur(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch in the current context: looked up with the
+// device current on the first call in each (device, context) and cached.
+// The first lookup may load this module's device code.
 xp_status noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return XP_ERR_LAUNCH;
   if (dev < 0 || dev >= kMaxDevices) return XP_ERR_UNSUPPORTED;
-  void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
-    if (p == nullptr) {
-      if (cudaGetSymbolAddress(&p, g_add_argmax_scratch) != cudaSuccess || p == nullptr) {
-        cudaGetLastError();  // do not leave the lookup's error for the next call to find
-        return XP_ERR_LAUNCH;
-      }
-      g_scratch_ptr[dev].store(p, std::memory_order_release);
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  ScratchEntry& e = g_scratch[dev];
+  unsigned long long id = current_ctx_id();  // 0 before the runtime has made a context current
+  if (id == 0 || e.ctx_id != id || e.ptr == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_add_argmax_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();  // do not leave the lookup's error for the next call to find
+      return XP_ERR_LAUNCH;
     }
+    // the lookup made the device's context current if none was
+    if (id == 0) id = current_ctx_id();
+    e.ptr = p;
+    e.ctx_id = id;  // an unreadable id (0) never matches: such calls look up again
   }
-  *out = p;
+  *out = e.ptr;
   return XP_OK;
 }
 }  // namespace

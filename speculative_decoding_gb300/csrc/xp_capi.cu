@@ -3,6 +3,8 @@
 // launchers.  See include/xpress.h for the contract of each call.
 #include <stdint.h>
 
+#include <atomic>
+
 #include "xp_common.cuh"
 #include "xp_internal.h"
 
@@ -14,18 +16,20 @@ bool aligned256(const void* p) { return ((uintptr_t)p & 255u) == 0; }
 // The kernels are compiled for sm_103a only; refuse other devices up front
 // rather than failing at launch.
 xp_status check_device() {
-  static int cached[64];  // 0 unknown, 1 ok, 2 unsupported
+  static std::atomic<int> cached[64];  // 0 unknown, 1 ok, 2 unsupported (any thread may fill it)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return XP_ERR_LAUNCH;
   if (dev < 0 || dev >= 64) return XP_ERR_UNSUPPORTED;
-  if (cached[dev] == 0) {
+  int c = cached[dev].load(std::memory_order_relaxed);
+  if (c == 0) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return XP_ERR_LAUNCH;
-    cached[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    c = (major == 10 && minor == 3) ? 1 : 2;
+    cached[dev].store(c, std::memory_order_relaxed);
   }
-  return cached[dev] == 1 ? XP_OK : XP_ERR_UNSUPPORTED;
+  return c == 1 ? XP_OK : XP_ERR_UNSUPPORTED;
 }
 
 }  // namespace

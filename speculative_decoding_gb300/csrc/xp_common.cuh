@@ -89,7 +89,7 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
-__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+__host__ __device__ constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct ArgmaxWs {
   WsHeader* hdr;
@@ -97,7 +97,7 @@ struct ArgmaxWs {
   unsigned int* cnt;
 };
 
-__host__ inline size_t argmax_ws_bytes(int64_t rows) {
+__host__ __device__ constexpr size_t argmax_ws_bytes(int64_t rows) {
   return 256 + align256(sizeof(unsigned long long) * (size_t)rows) + align256(4 * (size_t)rows);
 }
 __host__ inline ArgmaxWs argmax_ws(void* ws, int64_t rows) {

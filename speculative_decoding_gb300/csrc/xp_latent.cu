@@ -12,13 +12,15 @@
 // GB300 design.  The pages' kernel runs one program per block and makes one
 // SM pull all the weights; here the weights are spread over the whole GPU:
 //   proj_mix  : M tiles of whole blocks (128 rows) x 128 latent channels,
-//               the D-long reduction split over an 8-CTA cluster.  Warps 2..5
-//               gather the embedding rows of the previous tokens straight into
-//               128-byte-swizzled shared memory, warp 0 streams W_lat with TMA,
-//               warp 1 issues tcgen05.mma into TMEM.  The partial sums meet in
-//               distributed shared memory, summed in a fixed order; each CTA
-//               then adds the hidden cache and applies the causal mixer to
-//               its share of the blocks and writes u (fp32) and bf16(u).
+//               the D-long reduction split over S ordinary CTAs (no cluster).
+//               Warps 2..5 gather the embedding rows of the previous tokens
+//               straight into 128-byte-swizzled shared memory, warp 0 streams
+//               W_lat with TMA, warp 1 issues tcgen05.mma into TMEM.  Each CTA
+//               stores its fp32 partial tile to an L2-resident buffer; the S
+//               CTAs of a tile meet on an arrival counter and each sums the S
+//               partials of its own column slice in a fixed order, adds the
+//               hidden cache, applies the causal mixer and writes u (fp32)
+//               and bf16(u).
 //   mlp_up    : ub @ Wg and ub @ Wu as two TMEM accumulators over the same A
 //               tile; the epilogue applies SiLU(g) * v and rounds to bf16.
 //   mlp_down  : m @ Wd with the H-long reduction split over a cluster; the
@@ -625,8 +627,6 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
 // ============================================================================
 // mlp_down: lat = bf16(u + m @ Wd) for slots 1..B-1
 // ============================================================================
-// Shared memory: [0, region) is the stage ring, then red[128][tn + 4] (this
-// CTA's fp32 partial sums, read by the whole cluster); barriers after it.
 // Shared memory: [0, region) is the stage ring, then red[128][tn + 4] (this
 // CTA's fp32 partial sums, read by the whole cluster) reusing it; us (the
 // residual u of this CTA's w columns for the tile's 128 rows, copied by TMA

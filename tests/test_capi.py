@@ -3,6 +3,7 @@ include/xpress.h declares, and rejects bad arguments on the host before any
 CUDA call (so these checks run on a CPU-only machine)."""
 
 import ctypes
+import re
 
 import pytest
 
@@ -92,3 +93,24 @@ def test_schedule_entry_points_host_validation(L):
     assert _jp(L, ld=999) == xpress.XP_ERR_SHAPE        # ld_base < V
     assert _jp(L, ld=1004) == xpress.XP_ERR_ALIGN       # ld_base a multiple of 8
     assert _lp(L, N=0) == xpress.XP_OK                  # empty: no-op
+
+
+def test_readout_weight_parameter_is_named_transposed():
+    """The readout weight crosses the boundary vocabulary-major ([V, R], the
+    pages' W2 [R, V] transposed).  A raw pointer carries no shape, so the
+    parameter's name is what tells a caller: every declaration that takes it
+    must call it d_W2t, and its comment must state the [V,R] layout."""
+    text = open(xpress.HEADER).read()
+    decls = re.findall(r"XP_API[^;]*?\b(xp_\w+)\s*\(([^;]*?)\);", text, flags=re.S)
+    takers = {}
+    for name, params in decls:
+        w2 = re.findall(r"\b(d_W2\w*)\b", params)
+        if w2:
+            takers[name] = w2
+    assert {"xp_readout_argmax", "xp_jacobi_pass", "xp_jacobi_pass_ex", "xp_jacobi_fixpoint"} <= set(takers)
+    for name, params in takers.items():
+        assert params == ["d_W2t"], (name, params)
+        # the comment block right above the declaration names the layout
+        head = text[:text.index(f"{name}(")]
+        block = head[head.rindex("/*"):]
+        assert "d_W2t" in block and "[V,R]" in block, name

@@ -43,8 +43,9 @@ class Pass:
 
 
 def check_rows(orc, d, blk_in, blk_out, rows):
-    """BASELINE rule on the given rows; returns how many tokens were exactly
-    the oracle's."""
+    """The token rule on the given rows: each token equals the oracle's, or
+    its oracle logit lies within 0.0625 of the oracle row maximum.  Returns
+    how many tokens were exactly the oracle's."""
     lat = orc.latent(blk_in, d["am1"], d["hcache"], d["E"], d["W_lat"], d["L"], d["Wg"], d["Wu"], d["Wd"])
     B = blk_in.shape[1]
     R = lat.shape[-1]
@@ -59,6 +60,28 @@ def check_rows(orc, d, blk_in, blk_out, rows):
     return exact
 
 
+def oracle_pass(orc, d, blk_in):
+    """The oracle's own pass on a copy of blk_in."""
+    o = blk_in.copy()
+    orc.jacobi_pass(o, d["am1"], d["hcache"], d["E"], d["W_lat"], d["L"], d["Wg"], d["Wu"], d["Wd"], d["W2"],
+                    d["base"])
+    return o
+
+
+def check_all_rows(orc, d, blk_in, blk_out):
+    """Every row of one GPU pass against the oracle run on the same input
+    (teacher forcing): slot 0 untouched; each token equal to the oracle's, or
+    (a near-tie) its oracle logit within 0.0625 of the row maximum.  Returns
+    the oracle's blk and the rows whose token differs from the oracle's."""
+    np.testing.assert_array_equal(blk_out[:, 0], blk_in[:, 0])
+    o = oracle_pass(orc, d, blk_in)
+    B = blk_in.shape[1]
+    diff = [int(n) * (B - 1) + int(j) for n, j in np.argwhere(o[:, 1:] != blk_out[:, 1:])]
+    if diff:
+        assert check_rows(orc, d, blk_in, blk_out, diff) == 0
+    return o, diff
+
+
 SHAPES = [synth.TINY, synth.PassShape("p1", 9, 16, 3000, 256, 128, 256, 31),
           synth.PassShape("p2", 4, 5, 1000, 128, 64, 128, 32),
           synth.PassShape("pdr", 5, 16, 2000, 256, 256, 256, 33)]  # D = R, the pages' layout
@@ -69,68 +92,149 @@ def test_pass_parity(orc, shape):
     d = synth.pass_inputs(shape)
     p = Pass(d, shape)
     out, changed = p.run(d["blk"])
-    np.testing.assert_array_equal(out[:, 0], d["blk"][:, 0])
     assert changed == int((out != d["blk"]).sum())
-    exact = check_rows(orc, d, d["blk"], out, range(shape.rows))
-    assert exact >= shape.rows - max(1, shape.rows // 50)
-
-
-def test_multipass_teacher_forced_and_fixpoint(orc):
-    """Jacobi iteration to a fixpoint (base scaled down so the readout moves
-    tokens): every pass checked against the oracle on the GPU's own input;
-    the causal invariant (slots 1..p final after pass p) holds on the GPU; and
-    the untouched oracle run reaches its fixpoint in the same number of
-    passes when no near-tie intervened."""
-    shape = synth.PassShape("fp", 6, 8, 2000, 128, 64, 128, 41)
-    d = synth.pass_inputs(shape)
-    d["base"] = synth.to_bf16_bits(_f(d["base"]) * np.float32(0.05))
-    d["W2"] = synth.to_bf16_bits(_f(d["W2"]) * np.float32(8.0))
-    p = Pass(d, shape)
-    blk = d["blk"].copy()
-    hist = [blk.copy()]
-    counts = []
-    for _ in range(shape.B + 1):
-        out, changed = p.run(blk)
-        check_rows(orc, d, blk, out, range(shape.rows))
-        counts.append(changed)
-        hist.append(out.copy())
-        blk = out
-        if changed == 0:
-            break
-    assert counts[-1] == 0 and len(counts) <= shape.B
-    for q in range(1, len(hist)):
-        for r in range(q, len(hist)):
-            np.testing.assert_array_equal(hist[r][:, 1:q + 1], hist[q][:, 1:q + 1])
-    passes, ocounts = orc.jacobi_to_fixpoint(d["blk"].copy(), d["am1"], d["hcache"], d["E"], d["W_lat"], d["L"],
-                                             d["Wg"], d["Wu"], d["Wd"], d["W2"], d["base"], max_passes=shape.B + 1)
-    if np.array_equal(hist[-1], _oracle_final(orc, d, passes)):
-        assert passes == len(counts)
-
-
-def _oracle_final(orc, d, passes):
-    blk = d["blk"].copy()
-    for _ in range(passes):
-        orc.jacobi_pass(blk, d["am1"], d["hcache"], d["E"], d["W_lat"], d["L"], d["Wg"], d["Wu"], d["Wd"], d["W2"],
-                        d["base"])
-    return blk
+    _, diff = check_all_rows(orc, d, d["blk"], out)
+    assert len(diff) <= max(1, shape.rows // 50)
 
 
 def _f(h):
     return (np.asarray(h, np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
-def test_full_size_pass_sampled(orc):
-    """N=32, B=16, V=152064, D=3584, R=512, H=1536: every token of slot 1 of
-    every block plus sampled rows checked against the oracle's row logits."""
+def _trajectory(p, blk0, cap):
+    """Host loop of single GPU passes: [blk0, after pass 1, ...], stopping
+    after the first pass that changed nothing or after cap passes; plus each
+    pass's changed count."""
+    hist, counts = [blk0.copy()], []
+    while len(counts) < cap:
+        out, changed = p.run(hist[-1])
+        assert changed == int((out != hist[-1]).sum())
+        hist.append(out)
+        counts.append(changed)
+        if changed == 0:
+            break
+    return hist, counts
+
+
+def _exact_pass_inputs(N=4, B=8, V=1000, D=64, R=64, H=64, seed=5):
+    """A pass whose every floating-point result is exact on both sides, so the
+    GPU's tokens are the oracle's bit for bit and a multi-pass trajectory
+    cannot drift: E, W_lat, hcache are small integers over 4 (x = hcache +
+    e @ W_lat is a multiple of 1/16 below 32); the mixer weights are powers of
+    two (row b: 1/2, 1/4, ..., 2^-b, 2^-b, permuted per channel), so u is a
+    multiple of 2^-11 below 32 (16 significant bits); Wg = 0, so m = 0 and
+    lat = bf16(u), a multiple of 2^-11; W2 holds integers over 16, so every
+    partial sum of lat @ W2 is a multiple of 2^-15 below 2^8 (23 bits).  No
+    sum ever rounds, whatever the order."""
+    rng = np.random.default_rng(seed)
+
+    def q(a):
+        return synth.to_bf16_bits(np.asarray(a, np.float32))
+
+    L = np.zeros((B, B, R), np.float32)
+    for b in range(B):
+        w = [2.0 ** -(k + 1) for k in range(b)] + [2.0 ** -b]  # sums to 1
+        for r in range(R):
+            for k, wt in enumerate(w):
+                L[b, (b - k + r) % (b + 1), r] = wt
+    return dict(E=q(rng.integers(-3, 4, (V, D)) / 4.0), W_lat=q(rng.integers(-2, 3, (D, R)) / 4.0),
+                hcache=q(rng.integers(-4, 5, (N, B, R)) / 4.0), L=L, Wg=np.zeros((R, H), np.uint16),
+                Wu=q(rng.integers(-2, 3, (R, H)) / 4.0), Wd=q(rng.integers(-2, 3, (H, R)) / 4.0),
+                W2=q(rng.integers(-2, 3, (R, V)) / 16.0), base=synth.normal_bf16(seed, 9, (N * (B - 1), V), 0.5),
+                am1=rng.integers(0, V, N).astype(np.int64), blk=rng.integers(0, V, (N, B)).astype(np.int64))
+
+
+def test_multipass_exact_arithmetic_matches_oracle_trajectory(orc):
+    """Jacobi passes to the fixpoint on exact-arithmetic inputs: every pass's
+    blk, the per-pass change counts and the pass count equal the oracle's own
+    untouched run (no near-tie can move either side), for the host loop of
+    single passes and for xp_jacobi_fixpoint."""
+    N, B, V, D, R, H = 4, 8, 1000, 64, 64, 64
+    shape = synth.PassShape("exact", N, B, V, D, R, H, 5)
+    d = _exact_pass_inputs(N, B, V, D, R, H)
+    cap = 2 * B
+    p = Pass(d, shape)
+    hist, counts = _trajectory(p, d["blk"], cap)
+    ohist, ocounts = [d["blk"].copy()], []
+    while len(ocounts) < cap:
+        o = oracle_pass(orc, d, ohist[-1])
+        ocounts.append(int((o != ohist[-1]).sum()))
+        ohist.append(o)
+        if ocounts[-1] == 0:
+            break
+    assert counts == ocounts
+    for q, (g, o) in enumerate(zip(hist, ohist)):
+        np.testing.assert_array_equal(g, o, err_msg=f"after pass {q}")
+    assert 2 < len(counts) <= B  # the input moves tokens for several passes, and converges (causal mixer)
+    got, passes, changed = _fixpoint_run(p, d["blk"], cap)
+    assert passes == len(ocounts) and changed == sum(ocounts)
+    np.testing.assert_array_equal(got, ohist[-1])
+
+
+def test_multipass_teacher_forced_and_fixpoint(orc):
+    """Jacobi iteration to a fixpoint on random inputs (base scaled down so
+    the readout moves tokens): every row of every pass checked against the
+    oracle on the GPU's own input; the per-pass change count equals the
+    oracle's on that input up to the near-tie rows of that pass (each can move
+    the count by one); the causal invariant (slots 1..p final after pass p)
+    holds on the GPU."""
+    shape = synth.PassShape("fp", 6, 8, 2000, 128, 64, 128, 41)
+    d = synth.pass_inputs(shape)
+    d["base"] = synth.to_bf16_bits(_f(d["base"]) * np.float32(0.05))
+    d["W2"] = synth.to_bf16_bits(_f(d["W2"]) * np.float32(8.0))
+    p = Pass(d, shape)
+    hist, counts = _trajectory(p, d["blk"], shape.B + 1)
+    assert counts[-1] == 0 and len(counts) <= shape.B
+    for q in range(1, len(hist)):
+        o, diff = check_all_rows(orc, d, hist[q - 1], hist[q])
+        oc = int((o != hist[q - 1]).sum())
+        assert abs(oc - counts[q - 1]) <= len(diff), (q, oc, counts[q - 1], diff)
+    for q in range(1, len(hist)):
+        for r in range(q, len(hist)):
+            np.testing.assert_array_equal(hist[r][:, 1:q + 1], hist[q][:, 1:q + 1])
+
+
+def test_full_size_pass_all_rows(orc):
+    """N=32, B=16, V=152064, D=3584, R=512, H=1536: every one of the 480 rows
+    against the oracle's pass on the same input."""
     shape = synth.SERVE
     d = synth.pass_inputs(shape)
     p = Pass(d, shape)
     out, changed = p.run(d["blk"])
-    np.testing.assert_array_equal(out[:, 0], d["blk"][:, 0])
-    rng = np.random.default_rng(7)
-    rows = sorted(set(list(range(0, shape.rows, 15)) + rng.choice(shape.rows, 16, replace=False).tolist()))
-    exact = check_rows(orc, d, d["blk"], out, rows)
-    assert exact >= len(rows) - 2
+    assert changed == int((out != d["blk"]).sum())
+    _, diff = check_all_rows(orc, d, d["blk"], out)
+    print(f"\nfull-size pass: {shape.rows - len(diff)}/{shape.rows} tokens equal to the oracle's; "
+          f"near-tie rows {diff}")
+    assert len(diff) <= shape.rows // 50
+
+
+def test_latency_floor_pass_direct_and_graph_replay(orc):
+    """N=1 at the serving dims (V=152064, D=3584, R=512, H=1536): one readout
+    pair whose second CTA holds only padding rows.  The pass called directly
+    and the same pass captured in a CUDA graph, replayed twice from the same
+    input, give the oracle's tokens (rule above) and each other's bit for bit
+    (the kernels are deterministic)."""
+    shape = synth.FLOOR
+    d = synth.pass_inputs(shape)
+    p = Pass(d, shape)
+    out, changed = p.run(d["blk"])
+    _, diff = check_all_rows(orc, d, d["blk"], out)
+    assert len(diff) <= 1
+    t = p.t
+    blk = dev(d["blk"].copy())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        xpress.jacobi_pass(blk, p.am1, t["hcache"], t["E"], t["W_lat"], p.L, t["Wg"], t["Wu"], t["Wd"], t["W2t"],
+                           t["base"], p.ws, changed=p.changed)
+    blk0 = dev(d["blk"].copy())
+    for rep in range(2):
+        blk.copy_(blk0)
+        p.changed.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(blk.cpu().numpy(), out, err_msg=f"replay {rep}")
+        assert int(p.changed.item()) == changed
+    assert xpress.read_error(p.ws) == 0
 
 
 def _fixpoint_run(p, blk_np, max_passes):
@@ -156,37 +260,48 @@ def test_fixpoint_driver_matches_pass_loop(cap):
     d["base"] = synth.to_bf16_bits(_f(d["base"]) * np.float32(0.05))
     d["W2"] = synth.to_bf16_bits(_f(d["W2"]) * np.float32(8.0))
     p = Pass(d, shape)
-    blk, n, total = d["blk"].copy(), 0, 0
-    while n < cap:
-        blk, changed = p.run(blk)
-        n += 1
-        total += changed
-        if changed == 0:
-            break
+    hist, counts = _trajectory(p, d["blk"], cap)
     got, passes, changed = _fixpoint_run(p, d["blk"], cap)
-    np.testing.assert_array_equal(got, blk)
-    assert passes == n and changed == total
+    np.testing.assert_array_equal(got, hist[-1])
+    assert passes == len(counts) and changed == sum(counts)
     if cap == 16:
-        assert n < cap  # this input converges within B passes
+        assert len(counts) < cap  # this input converges within B passes
 
 
-def test_fixpoint_full_size_eight_passes(orc):
+def test_fixpoint_multipass_workload_vs_oracle(orc):
     """The multi-pass workload: N=64, B=16, V=152064, D=3584, R=512, H=1536,
-    at most 8 passes.  Same blk and count as the host pass loop; the count
-    equals the oracle's when its trajectory is the GPU's (teacher-forced
-    check of the last pass on sampled rows)."""
+    at most 8 passes.
+      * xp_jacobi_fixpoint gives the host pass loop's blk and pass count;
+      * every row of every GPU pass is checked against the oracle on the
+        GPU's own input (teacher forcing), and each pass's change count equals
+        the oracle's on that input up to that pass's near-tie rows;
+      * the oracle's own untouched run to its fixpoint: its pass count and
+        final blk equal the GPU's whenever no near-tie moved the GPU's
+        trajectory; a near-tie that did is shown by the 0.0625 rule above."""
     shape = synth.FIXPOINT
+    cap = 8
     d = synth.pass_inputs(shape)
     p = Pass(d, shape)
-    blk, n, prev = d["blk"].copy(), 0, None
-    while n < 8:
-        prev = blk
-        blk, changed = p.run(blk)
-        n += 1
-        if changed == 0:
-            break
-    got, passes, _ = _fixpoint_run(p, d["blk"], 8)
-    np.testing.assert_array_equal(got, blk)
-    assert passes == n
-    rows = list(range(0, shape.rows, 37))
-    check_rows(orc, d, prev, blk, rows)
+    hist, counts = _trajectory(p, d["blk"], cap)
+    got, passes, _ = _fixpoint_run(p, d["blk"], cap)
+    np.testing.assert_array_equal(got, hist[-1])
+    assert passes == len(counts)
+    near = []
+    ohist, ocounts = [d["blk"].copy()], []
+    for q in range(1, len(hist)):
+        o, diff = check_all_rows(orc, d, hist[q - 1], hist[q])
+        oc = int((o != hist[q - 1]).sum())
+        assert abs(oc - counts[q - 1]) <= len(diff), (q, oc, counts[q - 1], diff)
+        near += [(q, r) for r in diff]
+        if np.array_equal(ohist[-1], hist[q - 1]) and len(ocounts) == q - 1 and (not ocounts or ocounts[-1]):
+            ohist.append(o)  # the untouched oracle had the GPU's input: same pass
+            ocounts.append(oc)
+    while len(ocounts) < cap and ocounts[-1] != 0:  # the oracle's run past a divergence
+        o = oracle_pass(orc, d, ohist[-1])
+        ocounts.append(int((o != ohist[-1]).sum()))
+        ohist.append(o)
+    print(f"\nmulti-pass workload: GPU {len(counts)} passes {counts}; oracle {len(ocounts)} passes {ocounts}; "
+          f"near-tie (pass, row) {near}")
+    if not near:
+        assert ocounts == counts
+        np.testing.assert_array_equal(ohist[-1], hist[-1])

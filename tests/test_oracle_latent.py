@@ -99,6 +99,30 @@ def test_mixer_cumulative_mean(orc):
         np.testing.assert_allclose(u[:, b, :], want, rtol=1e-12, atol=1e-12)
 
 
+def test_mixer_channel_varying_selector(orc):
+    """W_lat = 0 and a mixer that differs per channel: L[b, j, r] = 1 when
+    j == r mod (b+1), else 0, so u[n, b, r] = hcache[n, r mod (b+1), r].  Each
+    channel r of slot b picks a different earlier slot, so a mixer that lost
+    the channel index (L[b, j, 0] for every r), or read L[j, b] instead of
+    L[b, j], gives another answer."""
+    d, sh = _case(seed=7, N=3, B=7, R=32)
+    d["W_lat"][:] = 0
+    B, R = sh.B, sh.R
+    L = np.zeros((B, B, R), np.float32)
+    for b in range(B):
+        for r in range(R):
+            L[b, r % (b + 1), r] = 1.0
+    _, u = orc.latent(d["blk"], d["am1"], d["hcache"], d["E"], d["W_lat"], L, d["Wg"], d["Wu"],
+                      d["Wd"], want_u=True)
+    hc = _f(d["hcache"])
+    for b in range(B):
+        for r in range(R):
+            np.testing.assert_array_equal(u[:, b, r], hc[:, r % (b + 1), r], err_msg=f"b={b} r={r}")
+    # the selector is not symmetric in (b, j) and not constant over r
+    assert not np.array_equal(L, L.transpose(1, 0, 2))
+    assert not np.array_equal(L[:, :, 0:1].repeat(R, axis=2), L)
+
+
 def test_mixer_is_causal(orc):
     """Changing slot j's inputs never changes u[b] for b < j."""
     d, sh = _case(seed=4, N=2, B=6)
