@@ -56,8 +56,9 @@ __device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float((uint
 // Shared memory: [0, region) is the stage ring; once the MMAs are done it holds
 // the S partial-sum slices of this CTA's w columns (TMA from the partial
 // buffer) and xs[128][w] (the reduced x), then the outgoing partial tile and,
-// once that is stored, the mixer output tiles us [rows][w] fp32 and ubs
-// [rows][w] bf16 (TMA-stored).  After it: Ls (the mixer weights of those
+// once that is stored, in the same place, the mixer output tiles us [rows][w]
+// fp32 and ubs [rows][w] bf16 (TMA-stored); that place is sized for the
+// larger of the two.  After it: Ls (the mixer weights of those
 // columns, the [B][B] square), hcs (the hidden cache of
 // those columns for the tile's 128 rows), the token table and the barriers.
 //
@@ -967,9 +968,11 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     p.r_pad = t.r_pad;
     const uint32_t stage_bytes = LT_A_CHUNK + (uint32_t)t.tn * LT_BK * 2;
     // after the MMAs the ring holds the S partial slices, xs and (1024-byte
-    // aligned) the outgoing partial tile
-    const size_t sl_xs =
-        (((size_t)(t.S + 1) * LT_BM * t.w * 4 + 1023) & ~size_t(1023)) + (size_t)LT_BM * t.tn * 4;
+    // aligned) the outgoing partial tile, whose place the mixer's output
+    // tiles (us fp32 and ubs bf16, w columns each) take later: the larger of
+    // the two (with S = 1 the mixer output is the larger)
+    const size_t pst_bytes = (size_t)LT_BM * (size_t)(t.tn * 4 > t.w * 6 ? t.tn * 4 : t.w * 6);
+    const size_t sl_xs = (((size_t)(t.S + 1) * LT_BM * t.w * 4 + 1023) & ~size_t(1023)) + pst_bytes;
     const size_t ls = proj_ls_bytes((int)B, t.w);
     const size_t hc = ((size_t)LT_BM * t.w * 2 + 127) & ~size_t(127);
     // the gathering warps keep stages - 1 stages in flight
@@ -1005,8 +1008,10 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
       return XP_ERR_LAUNCH;
     void* args[] = {&mapWlat, &mapHc, &mapPart, &mapPartSt, &mapL, &mapU, &mapUbS, &p};
     if (launch_ex((const void*)proj_mix_kernel, dim3((unsigned)(t.mtiles * t.ntiles * t.S)), smem, stream, 1, args) !=
-        cudaSuccess)
+        cudaSuccess) {
+      (void)cudaGetLastError();  // a failed launch must not be reported again by a later call
       return XP_ERR_LAUNCH;
+    }
   }
   // ---- mlp_up
   {
@@ -1028,9 +1033,10 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
       return XP_ERR_LAUNCH;
     void* args[] = {&mapUb, &mapWg, &mapWu, &p};
     const void* up_fn = do_mlp ? (const void*)mlp_up_kernel<false> : (const void*)mlp_up_kernel<true>;
-    if (launch_ex(up_fn, dim3((unsigned)(mtiles * p.htiles)), smem, stream, 1, args) !=
-        cudaSuccess)
+    if (launch_ex(up_fn, dim3((unsigned)(mtiles * p.htiles)), smem, stream, 1, args) != cudaSuccess) {
+      (void)cudaGetLastError();
       return XP_ERR_LAUNCH;
+    }
   }
   // ---- mlp_down
   {
@@ -1072,9 +1078,10 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
       return XP_ERR_LAUNCH;
     void* args[] = {&mapM, &mapWd, &mapU, &p};
     const void* down_fn = do_mlp ? (const void*)mlp_down_kernel<false> : (const void*)mlp_down_kernel<true>;
-    if (launch_ex(down_fn, dim3((unsigned)(mtiles * p.ntiles * p.S)), smem, stream, p.S, args) !=
-        cudaSuccess)
+    if (launch_ex(down_fn, dim3((unsigned)(mtiles * p.ntiles * p.S)), smem, stream, p.S, args) != cudaSuccess) {
+      (void)cudaGetLastError();
       return XP_ERR_LAUNCH;
+    }
   }
   return XP_OK;
 }

@@ -610,8 +610,11 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, readout_argmax_kernel, mapW2, mapBase, mapLat, p) != cudaSuccess) return XP_ERR_LAUNCH;
-  return cudaGetLastError() == cudaSuccess ? XP_OK : XP_ERR_LAUNCH;
+  if (cudaLaunchKernelEx(&cfg, readout_argmax_kernel, mapW2, mapBase, mapLat, p) != cudaSuccess) {
+    (void)cudaGetLastError();  // a failed launch must not be reported again by a later call
+    return XP_ERR_LAUNCH;
+  }
+  return XP_OK;
 }
 
 }  // namespace xp

@@ -153,6 +153,45 @@ def pass_activations(shape: PassShape) -> dict:
                 am1=tokens(s, _S["am1"], (N,), V), blk=tokens(s, _S["blk"], (N, B), V))
 
 
+def exact_mixer(B: int, R: int) -> np.ndarray:
+    """A folded mixer of powers of two: row b of channel r puts 1 (b = 0),
+    1/2 1/2 (b = 1), 1/2 1/4 1/4 (b = 2) or 1/2 1/4 1/8 1/8 (b >= 3) on
+    the distinct slots j = (r + k) mod (b+1), k = 0, 1, ...; zero elsewhere.
+    Rows sum to 1 exactly and differ from channel to channel."""
+    L = np.zeros((B, B, R), np.float32)
+    for b in range(B):
+        w = {0: [1.0], 1: [0.5, 0.5], 2: [0.5, 0.25, 0.25]}.get(b, [0.5, 0.25, 0.125, 0.125])
+        for r in range(R):
+            for k, wt in enumerate(w):
+                L[b, (r + k) % (b + 1), r] = wt
+    return L
+
+
+def exact_pass_inputs(shape: PassShape) -> dict:
+    """Pass inputs on which every sum of the method is exact in fp32 (so any
+    correct summation order gives the same bits): E holds integers in [-3, 3]
+    over 4 and W_lat integers in [-2, 2] over 4, so x = hcache + e @ W_lat is
+    a multiple of 1/16 (hcache: integers in [-4, 4] over 4); the mixer is
+    exact_mixer, so u is a multiple of 2^-7; Wg = 0, so m = 0 and
+    lat = bf16(u), again a multiple of 2^-7; W2 holds integers in [-2, 2] over
+    16, so every partial sum of lat @ W2 is a multiple of 2^-11 (exact while
+    below 2^13).  Magnitudes stay far inside those bounds for the shapes the
+    tests use.  base ~ N(0, 0.5) (the bias then moves tokens); am1 and blk
+    ~ U[0, V)."""
+    N, B, V, D, R, H, seed = shape.N, shape.B, shape.V, shape.D, shape.R, shape.H, shape.seed
+    g = np.random.Generator(np.random.Philox(np.random.SeedSequence([seed, 31])))
+
+    def q(a):
+        return to_bf16_bits(np.asarray(a, np.float32))
+
+    return dict(E=q(g.integers(-3, 4, (V, D)) / 4.0), W_lat=q(g.integers(-2, 3, (D, R)) / 4.0),
+                hcache=q(g.integers(-4, 5, (N, B, R)) / 4.0), L=exact_mixer(B, R),
+                Wg=np.zeros((R, H), np.uint16), Wu=q(g.integers(-2, 3, (R, H)) / 4.0),
+                Wd=q(g.integers(-2, 3, (H, R)) / 4.0), W2=q(g.integers(-2, 3, (R, V)) / 16.0),
+                base=normal_bf16(seed, _S["base"], (N * (B - 1), V), 0.5),
+                am1=g.integers(0, V, N).astype(np.int64), blk=g.integers(0, V, (N, B)).astype(np.int64))
+
+
 def plant_ties(base: np.ndarray, bias: np.ndarray, frac: float, seed: int, min_rows: int = 1):
     """Plant duplicated row maxima, in place.
 

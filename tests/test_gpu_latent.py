@@ -60,6 +60,26 @@ def test_latent_parity(orc, shape):
     assert np.mean(np.abs(g - w) <= np.abs(w) * 2**-7 + 1e-6) > 0.97
 
 
+# exact-arithmetic inputs (synth.exact_pass_inputs): every sum is exact in
+# fp32 whatever its order, so the latent must equal the oracle's bit for bit
+EXACT_SHAPES = [
+    synth.PassShape("e1", 4, 8, 1000, 64, 64, 64, 5),          # D = 64: the projection's D sum is not split
+    synth.PassShape("e3", 9, 16, 3000, 256, 128, 256, 7),
+    synth.PassShape("e4", 32, 16, 4096, 3584, 512, 1536, 8),   # the serving dims (E's vocab reduced)
+    synth.PassShape("e5", 1, 16, 4096, 3584, 512, 1536, 9),    # one block at the serving dims
+]
+
+
+@pytest.mark.parametrize("shape", EXACT_SHAPES, ids=[s.name for s in EXACT_SHAPES])
+def test_latent_exact_arithmetic_bit_exact(orc, shape):
+    d = synth.exact_pass_inputs(shape)
+    got, err = run_latent(d, shape)
+    assert err == 0
+    want = oracle_latent(orc, d)
+    bad = np.argwhere(got != want)
+    assert len(bad) == 0, (len(bad), bad[:8].tolist())
+
+
 def test_identity_path_exact(orc):
     """W_lat = 0, L = I, Wd = 0: lat[n, b-1] = hcache[n, b] bit for bit."""
     shape = synth.PassShape("id", 4, 6, 300, 128, 64, 64, 21)

@@ -119,29 +119,9 @@ def _trajectory(p, blk0, cap):
 def _exact_pass_inputs(N=4, B=8, V=1000, D=64, R=64, H=64, seed=5):
     """A pass whose every floating-point result is exact on both sides, so the
     GPU's tokens are the oracle's bit for bit and a multi-pass trajectory
-    cannot drift: E, W_lat, hcache are small integers over 4 (x = hcache +
-    e @ W_lat is a multiple of 1/16 below 32); the mixer weights are powers of
-    two (row b: 1/2, 1/4, ..., 2^-b, 2^-b, permuted per channel), so u is a
-    multiple of 2^-11 below 32 (16 significant bits); Wg = 0, so m = 0 and
-    lat = bf16(u), a multiple of 2^-11; W2 holds integers over 16, so every
-    partial sum of lat @ W2 is a multiple of 2^-15 below 2^8 (23 bits).  No
-    sum ever rounds, whatever the order."""
-    rng = np.random.default_rng(seed)
-
-    def q(a):
-        return synth.to_bf16_bits(np.asarray(a, np.float32))
-
-    L = np.zeros((B, B, R), np.float32)
-    for b in range(B):
-        w = [2.0 ** -(k + 1) for k in range(b)] + [2.0 ** -b]  # sums to 1
-        for r in range(R):
-            for k, wt in enumerate(w):
-                L[b, (b - k + r) % (b + 1), r] = wt
-    return dict(E=q(rng.integers(-3, 4, (V, D)) / 4.0), W_lat=q(rng.integers(-2, 3, (D, R)) / 4.0),
-                hcache=q(rng.integers(-4, 5, (N, B, R)) / 4.0), L=L, Wg=np.zeros((R, H), np.uint16),
-                Wu=q(rng.integers(-2, 3, (R, H)) / 4.0), Wd=q(rng.integers(-2, 3, (H, R)) / 4.0),
-                W2=q(rng.integers(-2, 3, (R, V)) / 16.0), base=synth.normal_bf16(seed, 9, (N * (B - 1), V), 0.5),
-                am1=rng.integers(0, V, N).astype(np.int64), blk=rng.integers(0, V, (N, B)).astype(np.int64))
+    cannot drift (the inputs come from synth.exact_pass_inputs, which states
+    the bounds; tests/test_synth.py checks them on the oracle's values)."""
+    return synth.exact_pass_inputs(synth.PassShape("exact", N, B, V, D, R, H, seed))
 
 
 def test_multipass_exact_arithmetic_matches_oracle_trajectory(orc):

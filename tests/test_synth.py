@@ -69,3 +69,27 @@ def test_pass_inputs_shapes_and_dtypes():
     act = synth.pass_activations(sh)
     for k in ("hcache", "base", "am1", "blk"):
         np.testing.assert_array_equal(act[k], d[k])
+
+
+@pytest.mark.parametrize("dims", [(4, 8, 1000, 64, 64, 64), (160, 16, 1000, 256, 512, 512),
+                                  (32, 16, 4096, 3584, 512, 1536)])
+def test_exact_inputs_keep_every_sum_exact(orc, dims):
+    """The bounds synth.exact_pass_inputs states, checked on the oracle's own
+    values: u (and so lat) on the 2^-7 grid with at most 24 significant bits,
+    and every partial sum of lat @ W2 on the 2^-11 grid below 2^13, so fp32
+    represents every intermediate exactly."""
+    shape = synth.PassShape("exact", *dims, 5)
+    d = synth.exact_pass_inputs(shape)
+    lat, u = orc.latent(d["blk"], d["am1"], d["hcache"], d["E"], d["W_lat"], d["L"], d["Wg"], d["Wu"], d["Wd"],
+                        want_u=True)
+    assert np.all(u * 2**7 == np.round(u * 2**7)) and np.abs(u).max() < 2**17
+    lf = orc.bf16_to_float(lat).astype(np.float64)
+    # m = 0 (Wg = 0): lat = bf16(u), which stays on the 2^-7 grid
+    np.testing.assert_array_equal(lat, orc.bf16_from_double(u[:, 1:, :]))
+    assert np.all(lf * 2**7 == np.round(lf * 2**7))
+    W2 = orc.bf16_to_float(d["W2"]).astype(np.float64)
+    assert np.all(W2 * 16 == np.round(W2 * 16))
+    assert (np.abs(lf.reshape(-1, shape.R)) @ np.abs(W2)).max() < 2**13
+    L = d["L"].astype(np.float64)
+    np.testing.assert_array_equal(L.sum(axis=1), 1.0)
+    assert np.all(np.triu(np.ones((shape.B, shape.B)), 1)[:, :, None] * L == 0)
