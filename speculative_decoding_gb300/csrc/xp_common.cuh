@@ -79,8 +79,8 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
 // ---------------------------------------------------------------------------
 struct WsHeader {
   unsigned int err;         // XP_DEVERR_* bits
-  unsigned int done;        // CTAs of the current readout grid that finished
-  unsigned int where;       // reserved (zero)
+  unsigned int done;          // CTAs of the current readout grid that finished (fixpoint driver)
+  unsigned int pass_changed;  // slots the current pass changed (fixpoint driver)
   // xp_jacobi_fixpoint: nonzero once a pass changed no slot (the passes
   // launched after it exit at once), and the number of passes that ran
   unsigned int converged;
@@ -132,6 +132,13 @@ __host__ inline ProjTiling proj_tiling(int64_t N, int64_t B, int64_t D, int64_t 
   while (t.S * 2 <= t.chunks && t.S * 2 <= 16 && t.tn / (t.S * 2) >= 8 &&
          (int64_t)t.mtiles * t.ntiles * t.S * 2 <= 128)
     t.S *= 2;
+  // with the D sum unsplit (many output tiles) a CTA mixes all its tile's
+  // channels: 64-channel tiles keep its shared memory (the mixer weights
+  // and the x / u / bf16(u) tiles of those channels) within budget
+  if (t.S == 1 && t.tn == 128) {
+    t.tn = 64;
+    t.ntiles = (int32_t)((R + t.tn - 1) / t.tn);
+  }
   t.w = t.tn / t.S;
   t.rows_pad = (int64_t)t.mtiles * 128;
   t.r_pad = (int64_t)t.ntiles * t.tn;

@@ -992,6 +992,7 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     int st = per_cta < 6 ? (per_cta < 2 ? 2 : per_cta) : 6;
     size_t smem = layout(st);
     while (st > 2 && smem > kSmemBudget) smem = layout(--st);
+    if (smem > kSmemBudget) return XP_ERR_UNSUPPORTED;  // the tiling keeps every supported shape within it
     CUtensorMap mapWlat, mapHc, mapPart, mapPartSt, mapL, mapU, mapUbS;
     if (!cached_map_bf16_2d(&mapWlat, W_lat, (uint64_t)R, (uint64_t)D, (uint64_t)R, 64, LT_BK) ||
         !cached_map_plain_2d(&mapHc, hcache, 2, (uint64_t)R, (uint64_t)(N * B), (uint64_t)R, (uint32_t)t.w, LT_BM) ||

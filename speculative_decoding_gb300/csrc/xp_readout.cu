@@ -22,8 +22,9 @@
 //     SM ingests thus serves 256 rows instead of 128, which halves the
 //     per-SM W2 traffic, the limit of this stream;
 //   * each CTA's 128 x R latent slice is staged ONCE into tensor memory (256
-//     columns for R = 512): TMA brings it into the (still empty) base ring and
-//     the epilogue warps copy their rows into TMEM lanes;
+//     columns for R = 512): one round of TMA brings it into the (still empty)
+//     base ring and second W2 slot, and the epilogue warps copy their rows
+//     into TMEM lanes (the second slot's first W2 tile is requested after);
 //   * the W2t half-tiles (64 vocab x R, up to eight 8 KB TMA boxes, one lane
 //     each) go into two tile slots, refilled by two producer warps (0 and 10,
 //     one slot each); the copies of both CTAs complete on the leader's
@@ -43,8 +44,9 @@
 //     '>' keeps the lowest index); both CTAs' epilogues release an
 //     accumulator on the leader's barrier;
 //   * each row's per-CTA winner is folded into a 64-bit (value, lowest
-//     index) key with atomicMax; the last CTA to finish writes blk, counts the
-//     changed slots and re-zeroes the keys.
+//     index) key with atomicMax and counted on the row's arrival counter; the
+//     arrival that completes a row writes its blk slot, counts a change and
+//     re-zeroes the key, so no CTA waits for the others at the end.
 #include "xp_common.cuh"
 #include "xp_internal.h"
 #include "xp_ptx.cuh"
@@ -69,7 +71,11 @@ constexpr int RO_SLOTS = 2;                            // slot t % 2 holds tile 
 constexpr uint32_t RO_BASE_BOX = RO_BM * 64 * 2;       // base box: 128 rows x 64 cols (16 KB)
 constexpr uint32_t RO_BASE_TILE = RO_BM * RO_BN * 2;   // 32 KB
 constexpr int RO_NBASE = 3;
-constexpr int RO_A_ROUND = 2 * RO_NBASE;                 // latent boxes per staging round (the base ring's 16 KB boxes)
+// latent boxes per staging round: the still-empty base ring's six 16 KB
+// boxes and the second W2 slot's four (its first W2 tile is requested once
+// the latent has been copied to TMEM), so R <= 512 stages in one round
+constexpr int RO_A_IN_BASE = 2 * RO_NBASE;
+constexpr int RO_A_ROUND = RO_A_IN_BASE + (int)(RO_W2_SLOT / RO_BASE_BOX);
 constexpr uint32_t RO_TMEM_A = 0;                      // A: columns [0, 32*kch)
 constexpr uint32_t RO_TMEM_ACC = 256;                  // accumulators: [256, 384), [384, 512)
 
@@ -79,6 +85,7 @@ struct ReadoutParams {
   int64_t* blk;
   int32_t* changed;
   unsigned long long* keys;
+  unsigned int* rcnt;    // per-row arrival counters (zero between calls)
   WsHeader* hdr;
   const uint32_t* skip;  // nullable: see pass_skipped
   int32_t* passes_out;   // nullable: fixpoint pass count (with skip)
@@ -133,7 +140,11 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   uint64_t* a_full = drain + 1;  // [2]: latent rounds landed in the base ring
   uint64_t* a_free = a_full + 2;  // the epilogue warps copied a round to TMEM
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(a_free + 1);
-  __shared__ int s_last;
+  // where latent box b of a staging round lands
+  auto a_box = [&](int b) -> uint8_t* {
+    return b < RO_A_IN_BASE ? sBase + (size_t)b * RO_BASE_BOX
+                            : sB + RO_W2_SLOT + (size_t)(b - RO_A_IN_BASE) * RO_BASE_BOX;
+  };
   if (pass_skipped(p.skip, false)) return;  // both CTAs of a pair read the same flag
   if (threadIdx.x == 0) XP_TRACE_MARK(0);
 
@@ -214,7 +225,9 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       const uint32_t u = (uint32_t)t >> 1;
       int ok = 1;
       if (lane == 0) {
-        if (u >= 1 && !mbar_wait_cluster(&acc_full[pid], (u - 1) & 1)) ok = 0;
+        // the second slot holds latent boxes until they are in TMEM
+        if (t == 1 && p.kch > RO_A_IN_BASE && !mbar_wait(a_free, 0)) ok = 0;
+        else if (u >= 1 && !mbar_wait_cluster(&acc_full[pid], (u - 1) & 1)) ok = 0;
         else if (rank == 0) {
           mbar_arrive_expect_tx(&b_full[pid], 2u * (uint32_t)p.kch * RO_W2_BOX);
           ++w2_armed;
@@ -236,10 +249,10 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
     if (pid == 0 && lane == 0) XP_TRACE_MARK(7);
   } else if (warp == RO_WARP_BASE) {
     // ---------------- TMA producer: base tiles (two lanes, one box each) ----------------
-    // The latent tile (A) goes first, through the still-empty base ring:
-    // rounds of up to RO_A_ROUND 64-column boxes (the ring holds six 16 KB
-    // boxes), each round copied to TMEM by the epilogue warps before the ring
-    // is reused.
+    // The latent tile (A) goes first, through the still-empty base ring and
+    // second W2 slot: rounds of up to RO_A_ROUND 64-column boxes (one round
+    // for R <= 512), each copied to TMEM by the epilogue warps before the
+    // space is reused.
     const int rounds = (p.kch + RO_A_ROUND - 1) / RO_A_ROUND;
     bool a_dead = false;
     const uint64_t pol_base = policy_evict_first();  // read once per pass
@@ -263,8 +276,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
         break;
       }
       if (lane < nbox)
-        tma_load_2d(sBase + (size_t)lane * RO_BASE_BOX, &mapLat, (RO_A_ROUND * r + lane) * 64, m_tile * RO_BM,
-                    &a_full[r]);
+        tma_load_2d(a_box(lane), &mapLat, (RO_A_ROUND * r + lane) * 64, m_tile * RO_BM, &a_full[r]);
       lat_issued = r + 1;
     }
     {
@@ -366,7 +378,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
           for (int j = 0; j < RO_A_ROUND / 2; ++j) {
             const int box = 2 * j + h, kc = RO_A_ROUND * r + box;
             if (kc < p.kch) {
-              const uint8_t* src = sBase + (size_t)box * RO_BASE_BOX + (size_t)rr * 128;
+              const uint8_t* src = a_box(box) + (size_t)rr * 128;
               uint32_t v[32];
 #pragma unroll
               for (int c = 0; c < 8; ++c) {
@@ -442,8 +454,31 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       }
       if (threadIdx.x == 64 && t < 16) XP_TRACE_MARK(10 + t);
     }
-    if (row_ok && bidx >= 0 && !dead) atomicMax(&p.keys[row], make_key(best, (uint32_t)bidx));
-    __threadfence();
+    // Fold this (row, half) winner into the row's key, then count the
+    // arrival: the 2 * per arrivals of a row (both halves of every vocab
+    // range) complete it, and the thread whose arrival does publishes the row
+    // and re-zeroes its key and counter; no CTA waits for the others.  A
+    // thread whose wait timed out still arrives (the row completes; the
+    // error bit is set).
+    if (row_ok) {
+      if (bidx >= 0 && !dead) atomicMax(&p.keys[row], make_key(best, (uint32_t)bidx));
+      __threadfence();
+      if (atomicAdd(&p.rcnt[row], 1u) == 2u * (uint32_t)p.per - 1u) {
+        __threadfence();
+        const unsigned long long k = atomicExch(&p.keys[row], 0ull);
+        p.rcnt[row] = 0u;
+        const int64_t idx = (int64_t)key_index(k);
+        const int64_t n = row / (p.B - 1), jj = row - n * (p.B - 1);
+        int64_t* slot = p.blk + n * p.B + 1 + jj;
+        if (p.changed != nullptr || p.passes_out != nullptr) {
+          if (*slot != idx) {
+            if (p.changed) atomicAdd(p.changed, 1);
+            if (p.passes_out) atomicAdd(&p.hdr->pass_changed, 1u);
+          }
+        }
+        *slot = idx;
+      }
+    }
   }
 
   __syncwarp();  // lane-0 roles rejoin their warps before any .aligned op
@@ -473,48 +508,23 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
     tc_fence_after();
     tmem_dealloc_pair(tmem, 512);
   }
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned int prev = atomicAdd(&p.hdr->done, 1u);
-    s_last = (prev == gridDim.x - 1);
-  }
-  __syncthreads();
-  if (s_last) {
-    // every other CTA has folded its rows (atomicMax, fence, then the done
-    // counter this CTA saw complete): read the winners with plain L2 loads,
-    // two rows per thread in flight together, publish them and zero the keys
-    // for the next call.  The old slot value is read only when a caller
-    // counts changes.
-    __threadfence();
-    const bool count = p.changed != nullptr || p.passes_out != nullptr;
-    int nchanged = 0;
-    auto publish = [&](int r, unsigned long long k) {
-      const int64_t idx = (int64_t)key_index(k);
-      const int64_t n = r / (p.B - 1), jj = r - n * (p.B - 1);
-      int64_t* slot = p.blk + n * p.B + 1 + jj;
-      if (count) nchanged += (*slot != idx);
-      *slot = idx;
-    };
-    for (int r0 = threadIdx.x; r0 < p.rows; r0 += 2 * blockDim.x) {
-      const int r1 = r0 + blockDim.x;
-      const unsigned long long k0 = __ldcg(&p.keys[r0]);
-      const unsigned long long k1 = r1 < p.rows ? __ldcg(&p.keys[r1]) : 0ull;
-      p.keys[r0] = 0ull;
-      if (r1 < p.rows) p.keys[r1] = 0ull;
-      publish(r0, k0);
-      if (r1 < p.rows) publish(r1, k1);
+  // Fixpoint driver only: the last CTA to finish counts the pass, and a pass
+  // that changed no slot is the last one (the passes launched after it exit
+  // at once).  Every row of the pass is published by then: each CTA counts
+  // itself after its threads' rows.
+  if (p.passes_out != nullptr) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(&p.hdr->done, 1u) == gridDim.x - 1) {
+        __threadfence();
+        const uint32_t np = p.hdr->passes + 1u;
+        p.hdr->passes = np;
+        *p.passes_out = (int32_t)np;
+        if (atomicExch(&p.hdr->pass_changed, 0u) == 0u) p.hdr->converged = 1u;
+        p.hdr->done = 0u;
+      }
     }
-    if (p.changed && nchanged) atomicAdd(p.changed, nchanged);
-    // fixpoint driver: count the pass; a pass that changed no slot is the
-    // last one (the passes launched after it exit at once)
-    const int any_changed = __syncthreads_or(nchanged);
-    if (p.passes_out && threadIdx.x == 0) {
-      const uint32_t np = p.hdr->passes + 1u;
-      p.hdr->passes = np;
-      *p.passes_out = (int32_t)np;
-      if (!any_changed) p.hdr->converged = 1u;
-    }
-    if (threadIdx.x == 0) p.hdr->done = 0u;
   }
   if (threadIdx.x == 0) XP_TRACE_MARK(6);
 }
@@ -593,6 +603,7 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
   p.blk = blk;
   p.changed = changed;
   p.keys = w.keys;
+  p.rcnt = w.cnt;
   p.hdr = w.hdr;
   p.skip = skip;
   p.passes_out = passes_out;

@@ -64,6 +64,7 @@ def test_latent_parity(orc, shape):
 # fp32 whatever its order, so the latent must equal the oracle's bit for bit
 EXACT_SHAPES = [
     synth.PassShape("e1", 4, 8, 1000, 64, 64, 64, 5),          # D = 64: the projection's D sum is not split
+    synth.PassShape("e2", 160, 16, 1000, 256, 512, 512, 6),    # 80 output tiles: not split either (64-channel tiles)
     synth.PassShape("e3", 9, 16, 3000, 256, 128, 256, 7),
     synth.PassShape("e4", 32, 16, 4096, 3584, 512, 1536, 8),   # the serving dims (E's vocab reduced)
     synth.PassShape("e5", 1, 16, 4096, 3584, 512, 1536, 9),    # one block at the serving dims
