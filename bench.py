@@ -406,6 +406,17 @@ def run_gb300(args, rank, world, local_rank):
         fx_reps = max(3, min(20, args.steps))
         fx_us = events_time(stream, fixpoint, fx_reps) / fx_reps
         fx_passes = int(x_passes.item())
+        # the same call captured in a CUDA graph: one conditional while node
+        # whose body is one pass, so only the passes needed run
+        fx_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(fx_graph):
+            fixpoint(0)
+        x_passes.zero_()
+        fx_graph.replay()
+        torch.cuda.synchronize()
+        if int(x_passes.item()) != fx_passes:
+            raise RuntimeError("the captured fixpoint ran a different number of passes")
+        fxg_us = events_time(stream, lambda i: fx_graph.replay(), fx_reps) / fx_reps
         if xpress.read_error(xws) != 0:
             raise RuntimeError("device-side error bits set in the multi-pass runs")
 
@@ -559,7 +570,9 @@ def run_gb300(args, rank, world, local_rank):
                           "median_us_single_replay": round(floor_med, 2)},
         "multipass": {"workload": "fixpoint N=64 B=16 V=152064 D=3584 R=512 H=1536, at most 8 passes",
                       "passes": fx_passes, "us_per_call": round(fx_us, 2),
-                      "us_per_pass": round(fx_us / max(1, fx_passes), 2)},
+                      "us_per_pass": round(fx_us / max(1, fx_passes), 2),
+                      "graph_us_per_call": round(fxg_us, 2),
+                      "graph_us_per_pass": round(fxg_us / max(1, fx_passes), 2)},
         "gemm_mlp": {"workload": sh.name + ", GEMM-MLP schedule (do_mlp = 0)", "us_per_pass": round(gm_us, 2)},
         "preprojected": {"workload": f"pass N={N} B={B} V={V} D={R} R={R} H={H} (E at the latent width)",
                          "us_per_pass": round(pp_us, 2),

@@ -261,10 +261,15 @@ XP_API xp_status xp_jacobi_pass_ex(int64_t* d_blk, const int64_t* d_am1, const x
  * counted).  Each pass reads the blk the previous one wrote
  * (_xpress_add_argmax_reduce_to_blk_kernel docstring).
  *
- * All max_passes passes are enqueued at once (4 launches each, plus two
- * small memsets), so the call is a fixed sequence of stream work (capturable
- * in a CUDA graph); the kernels of a pass enqueued after the fixpoint find the
- * workspace's convergence flag set and exit at their first instruction.
+ * On a stream that is not being captured, all max_passes passes are
+ * enqueued at once (4 launches each, plus two small memsets); the kernels of
+ * a pass enqueued after the fixpoint find the workspace's convergence flag
+ * set and exit at their first instruction.  On a stream that is being
+ * captured into a CUDA graph, the call adds the two memsets and one
+ * conditional while node whose body is one pass (captured on a private
+ * stream); the readout's last CTA sets the node's condition, so each launch
+ * of the graph runs exactly the passes needed.  Both forms give the same
+ * blk, *d_passes and *d_changed.
  * d_W2t: [V,R], the readout weight transposed, as in xp_jacobi_pass.
  * d_passes (device int32, required) receives the number of passes that ran;
  * d_changed (nullable, device int32) is incremented by the slots each pass

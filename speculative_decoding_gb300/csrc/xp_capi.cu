@@ -129,6 +129,64 @@ xp_status check_latent_args(const int64_t* blk, const int64_t* am1, const xp_bf1
   return XP_OK;
 }
 
+// xp_jacobi_fixpoint on a stream that is being captured: one conditional
+// while node whose body is one pass (the latent stage, then the readout in
+// fixpoint mode, which sets the node's handle), so the graph runs exactly the
+// passes the fixpoint needs.  The handle starts at 1 on every launch of the
+// graph; the counters the body reads were zeroed on `s` before this call.
+// The body is captured on a private stream in relaxed mode (the caller's
+// capture may be global).
+xp_status fixpoint_while_node(int64_t* blk, const int64_t* am1, const xp_bf16* hcache, const xp_bf16* E,
+                              const xp_bf16* W_lat, const float* L, const xp_bf16* Wg, const xp_bf16* Wu,
+                              const xp_bf16* Wd, uint16_t* lat, const xp_bf16* W2t, const xp_bf16* base,
+                              int64_t ld_base, int64_t N, int64_t B, int64_t V, int64_t D, int64_t R, int64_t H,
+                              int32_t max_passes, int32_t* passes, int32_t* changed, void* ws, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaGraph_t graph = nullptr;
+  const cudaGraphNode_t* deps = nullptr;
+  const cudaGraphEdgeData* edges = nullptr;
+  size_t ndeps = 0;
+  if (cudaStreamGetCaptureInfo(s, &cs, nullptr, &graph, &deps, &edges, &ndeps) != cudaSuccess ||
+      cs != cudaStreamCaptureStatusActive)
+    return XP_ERR_LAUNCH;
+  cudaGraphConditionalHandle handle;
+  if (cudaGraphConditionalHandleCreate(&handle, graph, 1, cudaGraphCondAssignDefault) != cudaSuccess)
+    return XP_ERR_LAUNCH;
+  cudaGraphNodeParams np = {};
+  np.type = cudaGraphNodeTypeConditional;
+  np.conditional.handle = handle;
+  np.conditional.type = cudaGraphCondTypeWhile;
+  np.conditional.size = 1;
+  cudaGraphNode_t node;
+  if (cudaGraphAddNode(&node, graph, deps, edges, ndeps, &np) != cudaSuccess) return XP_ERR_LAUNCH;
+  if (cudaStreamUpdateCaptureDependencies(s, &node, nullptr, 1, cudaStreamSetCaptureDependencies) != cudaSuccess)
+    return XP_ERR_LAUNCH;
+  cudaGraph_t body = np.conditional.phGraph_out[0];
+
+  cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+  if (cudaThreadExchangeStreamCaptureMode(&mode) != cudaSuccess) return XP_ERR_LAUNCH;
+  xp_status st = XP_OK;
+  cudaStream_t bs = nullptr;
+  if (cudaStreamCreateWithFlags(&bs, cudaStreamNonBlocking) != cudaSuccess) {
+    st = XP_ERR_LAUNCH;
+  } else {
+    if (cudaStreamBeginCaptureToGraph(bs, body, nullptr, nullptr, 0, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
+      st = XP_ERR_LAUNCH;
+    } else {
+      st = xp::launch_latent(blk, am1, hcache, E, W_lat, L, Wg, Wu, Wd, lat, N, B, V, D, R, H, ws, bs);
+      if (st == XP_OK)
+        st = xp::launch_readout_argmax(lat, W2t, base, ld_base, N * (B - 1), V, R, blk, B, changed, ws, bs, nullptr,
+                                       passes, (unsigned long long)handle, max_passes);
+      cudaGraph_t out = nullptr;
+      if (cudaStreamEndCapture(bs, &out) != cudaSuccess && st == XP_OK) st = XP_ERR_LAUNCH;
+    }
+    (void)cudaStreamDestroy(bs);
+  }
+  if (cudaThreadExchangeStreamCaptureMode(&mode) != cudaSuccess && st == XP_OK) st = XP_ERR_LAUNCH;
+  if (st != XP_OK) (void)cudaGetLastError();
+  return st;
+}
+
 }  // namespace
 
 extern "C" {
@@ -239,6 +297,11 @@ xp_status xp_jacobi_fixpoint(int64_t* d_blk, const int64_t* d_am1, const xp_bf16
     return XP_ERR_LAUNCH;
   if (N == 0) return XP_OK;
   uint16_t* lat = reinterpret_cast<uint16_t*>(static_cast<char*>(d_workspace) + lay.lat);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return XP_ERR_LAUNCH;
+  if (cs == cudaStreamCaptureStatusActive)
+    return fixpoint_while_node(d_blk, d_am1, d_hcache, d_E, d_W_lat, d_L, d_Wg, d_Wu, d_Wd, lat, d_W2t, d_base,
+                               ld_base, N, B, V, D, R, H, max_passes, d_passes, d_changed, d_workspace, s);
   const uint32_t* skip = &hdr->converged;
   for (int32_t k = 0; k < max_passes; ++k) {
     st = xp::launch_latent(d_blk, d_am1, d_hcache, d_E, d_W_lat, d_L, d_Wg, d_Wu, d_Wd, lat, N, B, V, D, R, H,

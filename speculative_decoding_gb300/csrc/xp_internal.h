@@ -21,12 +21,15 @@ xp_status launch_topc_argmax(const uint16_t* base_c, const uint16_t* bias_c, con
                              int64_t C, int64_t* blk, int64_t B, cudaStream_t stream);
 
 // skip (nullable): the pass's fixpoint flag (pass_skipped); passes_out
-// (nullable, with skip): the readout's last CTA counts the pass there and
-// sets the flag when the pass changed no slot.
+// (nullable): the readout's last CTA counts the pass there and sets the flag
+// when the pass changed no slot.  cond (with passes_out; 0 = none): the
+// handle of a captured while node, which the same CTA sets to continue while
+// the pass changed a slot and fewer than max_passes passes have run.
 xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const uint16_t* base, int64_t ld_base,
                                 int64_t rows, int64_t V, int64_t R, int64_t* blk, int64_t B, int32_t* changed,
                                 void* ws, cudaStream_t stream, const uint32_t* skip = nullptr,
-                                int32_t* passes_out = nullptr);
+                                int32_t* passes_out = nullptr, unsigned long long cond = 0,
+                                int32_t max_passes = 0);
 
 xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* hcache, const uint16_t* E,
                         const uint16_t* W_lat, const float* L, const uint16_t* Wg, const uint16_t* Wu,

@@ -88,7 +88,11 @@ struct ReadoutParams {
   unsigned int* rcnt;    // per-row arrival counters (zero between calls)
   WsHeader* hdr;
   const uint32_t* skip;  // nullable: see pass_skipped
-  int32_t* passes_out;   // nullable: fixpoint pass count (with skip)
+  int32_t* passes_out;   // nullable: fixpoint pass count
+  // nonzero: the while-node handle of a captured fixpoint loop; the last CTA
+  // sets it to 0 after the pass that changed nothing or the max_passes-th pass
+  unsigned long long cond;
+  int32_t max_passes;
 };
 
 // One 32-column chunk of one row: acc (fp32) -> bias = bf16(acc);
@@ -361,9 +365,10 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
 
     // Stage the A operand (this row of the latent, zero-padded to 64*kch)
     // into TMEM columns [0, 32*kch).  The latent arrives by TMA in the base
-    // ring, 128-byte swizzled (chunk c of row rr at (c ^ rr%8)*16), in rounds
-    // of up to six 64-column boxes; the two warps of a lane quadrant take
-    // alternate boxes.
+    // ring and the second W2 slot, 128-byte swizzled (chunk c of row rr at
+    // (c ^ rr%8)*16), in rounds of up to RO_A_ROUND 64-column boxes (one
+    // round when R <= 640); the two warps of a lane quadrant take alternate
+    // boxes.
     {
       const int rounds = (p.kch + RO_A_ROUND - 1) / RO_A_ROUND;
       bool ok = true;
@@ -510,8 +515,8 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
   }
   // Fixpoint driver only: the last CTA to finish counts the pass, and a pass
   // that changed no slot is the last one (the passes launched after it exit
-  // at once).  Every row of the pass is published by then: each CTA counts
-  // itself after its threads' rows.
+  // at once; in a captured loop, the while node stops).  Every row of the
+  // pass is published by then: each CTA counts itself after its threads' rows.
   if (p.passes_out != nullptr) {
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -521,8 +526,12 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
         const uint32_t np = p.hdr->passes + 1u;
         p.hdr->passes = np;
         *p.passes_out = (int32_t)np;
-        if (atomicExch(&p.hdr->pass_changed, 0u) == 0u) p.hdr->converged = 1u;
+        const bool last = atomicExch(&p.hdr->pass_changed, 0u) == 0u;
+        if (last) p.hdr->converged = 1u;
         p.hdr->done = 0u;
+        if (p.cond != 0ull)
+          cudaGraphSetConditional((cudaGraphConditionalHandle)p.cond,
+                                  (!last && (int32_t)np < p.max_passes) ? 1u : 0u);
       }
     }
   }
@@ -560,7 +569,8 @@ RoDevInfo g_ro_dev[64];
 
 xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const uint16_t* base, int64_t ld_base,
                                 int64_t rows, int64_t V, int64_t R, int64_t* blk, int64_t B, int32_t* changed,
-                                void* ws, cudaStream_t stream, const uint32_t* skip, int32_t* passes_out) {
+                                void* ws, cudaStream_t stream, const uint32_t* skip, int32_t* passes_out,
+                                unsigned long long cond, int32_t max_passes) {
   if (rows <= 0) return XP_OK;
   const int kch = (int)((R + 63) / 64);
   if (kch > RO_MAX_KCH) return XP_ERR_SHAPE;
@@ -607,6 +617,8 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
   p.hdr = w.hdr;
   p.skip = skip;
   p.passes_out = passes_out;
+  p.cond = cond;
+  p.max_passes = max_passes;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

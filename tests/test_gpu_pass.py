@@ -150,6 +150,9 @@ def test_multipass_exact_arithmetic_matches_oracle_trajectory(orc):
     got, passes, changed = _fixpoint_run(p, d["blk"], cap)
     assert passes == len(ocounts) and changed == sum(ocounts)
     np.testing.assert_array_equal(got, ohist[-1])
+    for got, passes, changed in _fixpoint_graph_runs(p, d["blk"], cap):
+        assert passes == len(ocounts) and changed == sum(ocounts)
+        np.testing.assert_array_equal(got, ohist[-1])
 
 
 def test_multipass_teacher_forced_and_fixpoint(orc):
@@ -230,6 +233,31 @@ def _fixpoint_run(p, blk_np, max_passes):
     return blk.cpu().numpy(), int(passes.item()), int(changed.item())
 
 
+def _fixpoint_graph_runs(p, blk_np, max_passes, replays=2):
+    """xp_jacobi_fixpoint captured in a CUDA graph (a conditional while node
+    whose body is one pass), replayed from blk_np several times: the list of
+    (blk, passes, changed) of each replay."""
+    blk = dev(blk_np.copy())
+    blk0 = dev(blk_np.copy())
+    passes = torch.zeros(1, dtype=torch.int32, device="cuda")
+    changed = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t = p.t
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        xpress.jacobi_fixpoint(blk, p.am1, t["hcache"], t["E"], t["W_lat"], p.L, t["Wg"], t["Wu"], t["Wd"],
+                               t["W2t"], t["base"], p.ws, passes, max_passes=max_passes, changed=changed)
+    out = []
+    for _ in range(replays):
+        blk.copy_(blk0)
+        changed.zero_()
+        passes.fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        out.append((blk.cpu().numpy(), int(passes.item()), int(changed.item())))
+    assert xpress.read_error(p.ws) == 0
+    return out
+
+
 @pytest.mark.parametrize("cap", [3, 16])
 def test_fixpoint_driver_matches_pass_loop(cap):
     """xp_jacobi_fixpoint (all passes enqueued, no host round trip) against the
@@ -247,6 +275,23 @@ def test_fixpoint_driver_matches_pass_loop(cap):
     assert passes == len(counts) and changed == sum(counts)
     if cap == 16:
         assert len(counts) < cap  # this input converges within B passes
+
+
+@pytest.mark.parametrize("cap", [1, 3, 16])
+def test_fixpoint_captured_while_node_matches_pass_loop(cap):
+    """xp_jacobi_fixpoint captured in a CUDA graph runs a conditional while
+    node (one pass per iteration, stopped by the readout's last CTA): every
+    replay gives the host pass loop's final blk, pass count and change count,
+    also when max_passes stops it before the fixpoint (cap 1 and 3)."""
+    shape = synth.PassShape("fp", 6, 8, 2000, 128, 64, 128, 41)
+    d = synth.pass_inputs(shape)
+    d["base"] = synth.to_bf16_bits(_f(d["base"]) * np.float32(0.05))
+    d["W2"] = synth.to_bf16_bits(_f(d["W2"]) * np.float32(8.0))
+    p = Pass(d, shape)
+    hist, counts = _trajectory(p, d["blk"], cap)
+    for got, passes, changed in _fixpoint_graph_runs(p, d["blk"], cap, replays=3):
+        np.testing.assert_array_equal(got, hist[-1])
+        assert passes == len(counts) and changed == sum(counts)
 
 
 def test_fixpoint_multipass_workload_vs_oracle(orc):
@@ -267,6 +312,9 @@ def test_fixpoint_multipass_workload_vs_oracle(orc):
     got, passes, _ = _fixpoint_run(p, d["blk"], cap)
     np.testing.assert_array_equal(got, hist[-1])
     assert passes == len(counts)
+    for got, passes, changed in _fixpoint_graph_runs(p, d["blk"], cap):
+        np.testing.assert_array_equal(got, hist[-1])
+        assert passes == len(counts) and changed == sum(counts)
     near = []
     ohist, ocounts = [d["blk"].copy()], []
     for q in range(1, len(hist)):
