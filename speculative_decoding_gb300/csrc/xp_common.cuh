@@ -118,6 +118,40 @@ struct ProjTiling {
   int32_t bpt, mtiles, tn, ntiles, chunks, S, w;
   int64_t rows_pad, r_pad;  // partial-sum buffer: [S][rows_pad][r_pad] fp32
 };
+
+// The projection kernel's dynamic shared memory for a tiling and a ring of
+// `stages` stages (128-row A chunks of 64 K columns plus a tn-wide W_lat
+// box each).  [0, region): the ring; after the MMAs the same place holds the
+// S partial slices and xs (w columns each), then the outgoing partial tile,
+// whose place the mixer's output (u fp32 and bf16(u), w columns) takes later:
+// the larger of the two.  Then the mixer weights of the w columns (the whole
+// [B][B] square), the hidden cache of those columns, the token table, and the
+// barriers (full/empty per stage, acc_full, aux_full, slice_full) and the TMEM
+// address slot; 1024 bytes of alignment slack in front.
+struct ProjSmem {
+  uint32_t region, hc_off, tok_off, bar_off;
+  size_t total;
+};
+__host__ inline ProjSmem proj_smem(const ProjTiling& t, int64_t B, int stages) {
+  constexpr size_t rows = 128;
+  const size_t stage_bytes = rows * 64 * 2 + (size_t)t.tn * 64 * 2;
+  const size_t pst = rows * (size_t)(t.tn * 4 > t.w * 6 ? t.tn * 4 : t.w * 6);
+  const size_t sl_xs = (((size_t)(t.S + 1) * rows * t.w * 4 + 1023) & ~size_t(1023)) + pst;
+  const size_t ls = ((size_t)(B * B * t.w * 4) + 127) & ~size_t(127);
+  const size_t hc = (rows * t.w * 2 + 127) & ~size_t(127);
+  const size_t ring = (size_t)stages * stage_bytes;
+  ProjSmem m;
+  m.region = (uint32_t)((ring > sl_xs ? ring : sl_xs + 1023) & ~size_t(1023));
+  m.hc_off = m.region + (uint32_t)ls;
+  m.tok_off = m.hc_off + (uint32_t)hc;
+  m.bar_off = m.tok_off + 8 * (uint32_t)rows;
+  m.total = 1024 + (size_t)m.bar_off + 8 * (2 * (size_t)stages + 3) + 16;
+  return m;
+}
+// Dynamic shared memory a latent-stage kernel may use: the 227 KB opt-in
+// maximum less the static shared memory and a margin.
+constexpr size_t kLatentSmemBudget = 226 * 1024;
+
 __host__ inline ProjTiling proj_tiling(int64_t N, int64_t B, int64_t D, int64_t R) {
   ProjTiling t;
   t.bpt = B <= 128 ? (int32_t)(128 / B) : 1;
@@ -132,14 +166,22 @@ __host__ inline ProjTiling proj_tiling(int64_t N, int64_t B, int64_t D, int64_t 
   while (t.S * 2 <= t.chunks && t.S * 2 <= 16 && t.tn / (t.S * 2) >= 8 &&
          (int64_t)t.mtiles * t.ntiles * t.S * 2 <= 128)
     t.S *= 2;
+  t.w = t.tn / t.S;
+  // fewer slices while a CTA's share of the epilogue (w columns of mixer
+  // weights, partial slices and mixer tiles) does not fit beside a two-stage
+  // ring
+  while (t.S > 1 && proj_smem(t, B, 2).total > kLatentSmemBudget) {
+    t.S /= 2;
+    t.w = t.tn / t.S;
+  }
   // with the D sum unsplit (many output tiles) a CTA mixes all its tile's
   // channels: 64-channel tiles keep its shared memory (the mixer weights
   // and the x / u / bf16(u) tiles of those channels) within budget
   if (t.S == 1 && t.tn == 128) {
     t.tn = 64;
     t.ntiles = (int32_t)((R + t.tn - 1) / t.tn);
+    t.w = t.tn;
   }
-  t.w = t.tn / t.S;
   t.rows_pad = (int64_t)t.mtiles * 128;
   t.r_pad = (int64_t)t.ntiles * t.tn;
   return t;

@@ -84,9 +84,6 @@ struct ProjParams {
   const uint32_t* skip;  // nullable: see pass_skipped
 };
 
-// the mixer weights of a CTA's w columns: the full [B][B] square (one TMA
-// box; entries above the diagonal are loaded and ignored)
-__host__ __device__ inline uint32_t proj_ls_bytes(int B, int w) { return (uint32_t)((B * B * w * 4 + 127) & ~127); }
 
 __global__ void __launch_bounds__(LT_THREADS, 1)
 proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_constant__ CUtensorMap mapHc,
@@ -869,6 +866,7 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
 namespace {
 
 bool g_lt_attr[64];
+int g_lt_sms[64];  // multiprocessors of each device (read with the attributes)
 
 cudaError_t launch_ex(const void* kernel_fn, dim3 grid, size_t smem, cudaStream_t stream, int cluster, void** args) {
   cudaLaunchConfig_t cfg = {};
@@ -899,9 +897,6 @@ int pow2_floor(int x, int cap) {
   return s;
 }
 
-// Dynamic shared memory a kernel here may use: the 227 KB opt-in maximum less
-// the static shared memory and a margin.
-constexpr size_t kSmemBudget = 226 * 1024;
 
 }  // namespace
 
@@ -914,7 +909,8 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return XP_ERR_LAUNCH;
   if (!g_lt_attr[dev]) {
     int max_smem = 0;
-    if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&g_lt_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return XP_ERR_LAUNCH;
     // the largest dynamic shared memory each kernel may ask for (the opt-in
     // maximum less its static shared memory) and the largest carve-out
@@ -966,33 +962,19 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     p.ntiles = t.ntiles;
     p.rows_pad = t.rows_pad;
     p.r_pad = t.r_pad;
-    const uint32_t stage_bytes = LT_A_CHUNK + (uint32_t)t.tn * LT_BK * 2;
-    // after the MMAs the ring holds the S partial slices, xs and (1024-byte
-    // aligned) the outgoing partial tile, whose place the mixer's output
-    // tiles (us fp32 and ubs bf16, w columns each) take later: the larger of
-    // the two (with S = 1 the mixer output is the larger)
-    const size_t pst_bytes = (size_t)LT_BM * (size_t)(t.tn * 4 > t.w * 6 ? t.tn * 4 : t.w * 6);
-    const size_t sl_xs = (((size_t)(t.S + 1) * LT_BM * t.w * 4 + 1023) & ~size_t(1023)) + pst_bytes;
-    const size_t ls = proj_ls_bytes((int)B, t.w);
-    const size_t hc = ((size_t)LT_BM * t.w * 2 + 127) & ~size_t(127);
-    // the gathering warps keep stages - 1 stages in flight
+    // the gathering warps keep stages - 1 stages in flight; as deep a ring as
+    // fits (at least 2 stages)
     const int per_cta = (t.chunks + t.S - 1) / t.S;
-    // Ls, hcs, the token table, then full/empty per stage, acc_full,
-    // aux_full, slice_full and the TMEM address slot; as deep a ring as fits
-    // (at least 2 stages)
-    auto layout = [&](int st) {
-      const size_t ring = (size_t)st * stage_bytes;
-      p.stages = st;
-      p.region = (uint32_t)((ring > sl_xs ? ring : sl_xs + 1023) & ~size_t(1023));
-      p.hc_off = p.region + (uint32_t)ls;
-      p.tok_off = p.hc_off + (uint32_t)hc;
-      p.bar_off = p.tok_off + 8 * LT_BM;
-      return 1024 + (size_t)p.bar_off + 8 * (2 * st + 3) + 16;
-    };
     int st = per_cta < 6 ? (per_cta < 2 ? 2 : per_cta) : 6;
-    size_t smem = layout(st);
-    while (st > 2 && smem > kSmemBudget) smem = layout(--st);
-    if (smem > kSmemBudget) return XP_ERR_UNSUPPORTED;  // the tiling keeps every supported shape within it
+    while (st > 2 && proj_smem(t, B, st).total > kLatentSmemBudget) --st;
+    const ProjSmem lay_s = proj_smem(t, B, st);
+    if (lay_s.total > kLatentSmemBudget) return XP_ERR_UNSUPPORTED;  // the tiling keeps every supported shape within it
+    p.stages = st;
+    p.region = lay_s.region;
+    p.hc_off = lay_s.hc_off;
+    p.tok_off = lay_s.tok_off;
+    p.bar_off = lay_s.bar_off;
+    const size_t smem = lay_s.total;
     CUtensorMap mapWlat, mapHc, mapPart, mapPartSt, mapL, mapU, mapUbS;
     if (!cached_map_bf16_2d(&mapWlat, W_lat, (uint64_t)R, (uint64_t)D, (uint64_t)R, 64, LT_BK) ||
         !cached_map_plain_2d(&mapHc, hcache, 2, (uint64_t)R, (uint64_t)(N * B), (uint64_t)R, (uint32_t)t.w, LT_BM) ||
@@ -1024,9 +1006,12 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     p.H = (int32_t)H;
     p.chunks = (int32_t)((R + LT_BK - 1) / LT_BK);
     p.htiles = (int32_t)(H / 64);
-    p.stages = p.chunks < 6 ? (p.chunks < 2 ? 2 : p.chunks) : 6;
-    const size_t smem = 1024 + (size_t)p.stages * (LT_A_CHUNK + 2 * LT_BOX) + 8 * (2 * p.stages + 1) + 16;
     const int mtiles = (rows + LT_BM - 1) / LT_BM;
+    p.stages = p.chunks < 6 ? (p.chunks < 2 ? 2 : p.chunks) : 6;
+    // more CTAs than SMs: a three-stage ring, so two CTAs fit on an SM and
+    // the grid runs in one wave
+    if ((int64_t)mtiles * p.htiles > g_lt_sms[dev] && p.stages > 3) p.stages = 3;
+    const size_t smem = 1024 + (size_t)p.stages * (LT_A_CHUNK + 2 * LT_BOX) + 8 * (2 * p.stages + 1) + 16;
     CUtensorMap mapUb, mapWg, mapWu;
     if (!cached_map_bf16_2d(&mapUb, ub, (uint64_t)R, (uint64_t)rows, (uint64_t)R, LT_BK, LT_BM) ||
         !cached_map_bf16_2d(&mapWg, Wg, (uint64_t)H, (uint64_t)R, (uint64_t)H, 64, LT_BK) ||
@@ -1067,11 +1052,14 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     // us, then full/empty per stage, acc_full, aux_full and the TMEM slot
     auto total = [&](int st) { return 1024 + region_of(st) + us_bytes + 8 * (2 * st + 2) + 16; };
     const int per_cta = (p.chunks + p.S - 1) / p.S;
+    const int mtiles = (rows + LT_BM - 1) / LT_BM;
     p.stages = per_cta < 6 ? (per_cta < 2 ? 2 : per_cta) : 6;
+    // more CTAs than SMs: a four-stage ring, so two CTAs fit on an SM and the
+    // grid runs in one wave
+    if ((int64_t)mtiles * p.ntiles * p.S > g_lt_sms[dev] && p.stages > 4) p.stages = 4;
     p.region = (uint32_t)region_of(p.stages);
     p.bar_off = p.region + (uint32_t)us_bytes;
     const size_t smem = total(p.stages);
-    const int mtiles = (rows + LT_BM - 1) / LT_BM;
     CUtensorMap mapM, mapWd, mapU;
     if (!cached_map_bf16_2d(&mapM, m, (uint64_t)H, (uint64_t)rows, (uint64_t)H, LT_BK, LT_BM) ||
         !cached_map_bf16_2d(&mapWd, Wd, (uint64_t)R, (uint64_t)H, (uint64_t)R, 64, LT_BK) ||

@@ -68,6 +68,8 @@ EXACT_SHAPES = [
     synth.PassShape("e3", 9, 16, 3000, 256, 128, 256, 7),
     synth.PassShape("e4", 32, 16, 4096, 3584, 512, 1536, 8),   # the serving dims (E's vocab reduced)
     synth.PassShape("e5", 1, 16, 4096, 3584, 512, 1536, 9),    # one block at the serving dims
+    synth.PassShape("e6", 96, 16, 1000, 256, 512, 512, 10),    # 12 M tiles: a 2-way D split would not fit, unsplit
+    synth.PassShape("e7", 64, 16, 1000, 256, 512, 1536, 11),   # MLP grids of 192 and 256 CTAs: two CTAs per SM
 ]
 
 

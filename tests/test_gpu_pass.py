@@ -85,7 +85,8 @@ def check_all_rows(orc, d, blk_in, blk_out):
 SHAPES = [synth.TINY, synth.PassShape("p1", 9, 16, 3000, 256, 128, 256, 31),
           synth.PassShape("p2", 4, 5, 1000, 128, 64, 128, 32),
           synth.PassShape("pdr", 5, 16, 2000, 256, 256, 256, 33),  # D = R, the pages' layout
-          synth.PassShape("n200", 200, 16, 4096, 512, 512, 256, 34)]  # 3000 rows: D sum unsplit, 12 readout pair rows
+          synth.PassShape("n200", 200, 16, 4096, 512, 512, 256, 34),  # 3000 rows: D sum unsplit, 12 readout pair rows
+          synth.PassShape("n96", 96, 16, 4096, 512, 512, 1536, 35)]  # 12 M tiles; MLP grids above the SM count
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=[s.name for s in SHAPES])
