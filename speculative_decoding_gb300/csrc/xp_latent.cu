@@ -79,6 +79,7 @@ struct ProjParams {
   uint32_t* cnt;
   WsHeader* hdr;
   int32_t N, B, V, D, R, bpt, tn, S, w, chunks, ntiles, stages;
+  int32_t prow;  // rows of a partial tile that are stored and summed (128, or fewer for a lone M tile)
   int64_t rows_pad, r_pad;
   uint32_t region, hc_off, tok_off, bar_off;
   const uint32_t* skip;  // nullable: see pass_skipped
@@ -275,7 +276,9 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
         cp_async_16(dst + r * 128 + ((piece ^ (r & 7)) << 4), ok ? p.E + t * p.D + kel : p.E, ok ? 16u : 0u);
       }
       cp_async_commit();
+      if (lane == 0 && gw == 0 && i == 0) XP_TRACE_MARK(26);
       if (i >= lag) {
+        if (lane == 0 && gw == 0 && i == lag) XP_TRACE_MARK(27);
         cp_async_wait_group_n(lag);
         hand_over(i - lag);
       }
@@ -340,7 +343,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
         __nanosleep(64);
       }
       fence_proxy_async_global();
-      if (ok) mbar_arrive_expect_tx(slice_full, (uint32_t)(p.S * LT_BM * p.w * 4));
+      if (ok) mbar_arrive_expect_tx(slice_full, (uint32_t)(p.S * p.prow * p.w * 4));
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) {
@@ -399,7 +402,21 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     // past R are clipped by the stores)
     float* us = reinterpret_cast<float*>(pst);                            // [bpt*B][w]
     uint16_t* ubs = reinterpret_cast<uint16_t*>(pst + (size_t)LT_BM * p.w * 4);  // [bpt*B][w]
-    for (int it = et; it < nbl * p.w; it += 128) {
+    if (nbl * p.w <= 16) {
+      // very few (block, channel) pairs (one block, a narrow slice): one
+      // output per thread, the same sum in the same order as below
+      for (int it = et; it < nbl * p.B * p.w; it += 128) {
+        const int bb = it / p.w, c = it - bb * p.w;  // bb = bl * B + b
+        const int bl = bb / p.B, b = bb - bl * p.B;
+        const float* Lb = Ls + (b * p.B) * p.w + c;
+        const float* xc = xs + (bl * p.B) * p.w + c;
+        float uu = 0.f;
+        for (int j = 0; j <= b; ++j) uu = fmaf(Lb[j * p.w], xc[j * p.w], uu);
+        const int o = bb * p.w + c;
+        us[o] = uu;
+        ubs[o] = (uint16_t)(f32x2_to_bf16x2(uu, 0.f) & 0xffffu);
+      }
+    } else for (int it = et; it < nbl * p.w; it += 128) {
       const int bl = it / p.w, c = it - bl * p.w;
       float x[LT_MAX_B];
 #pragma unroll
@@ -962,6 +979,8 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     p.ntiles = t.ntiles;
     p.rows_pad = t.rows_pad;
     p.r_pad = t.r_pad;
+    // a lone M tile stores and sums only the rows that hold blocks
+    p.prow = t.mtiles == 1 ? (int32_t)(((N * B + 7) / 8) * 8 < LT_BM ? ((N * B + 7) / 8) * 8 : LT_BM) : LT_BM;
     // the gathering warps keep stages - 1 stages in flight; as deep a ring as
     // fits (at least 2 stages)
     const int per_cta = (t.chunks + t.S - 1) / t.S;
@@ -979,9 +998,9 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     if (!cached_map_bf16_2d(&mapWlat, W_lat, (uint64_t)R, (uint64_t)D, (uint64_t)R, 64, LT_BK) ||
         !cached_map_plain_2d(&mapHc, hcache, 2, (uint64_t)R, (uint64_t)(N * B), (uint64_t)R, (uint32_t)t.w, LT_BM) ||
         !cached_map_plain_2d(&mapPart, p.part, 4, (uint64_t)t.r_pad, (uint64_t)(t.S * t.rows_pad), (uint64_t)t.r_pad,
-                             (uint32_t)t.w, LT_BM) ||
+                             (uint32_t)t.w, (uint32_t)p.prow) ||
         !cached_map_plain_2d(&mapPartSt, p.part, 4, (uint64_t)t.r_pad, (uint64_t)(t.S * t.rows_pad),
-                             (uint64_t)t.r_pad, 32, LT_BM, true) ||
+                             (uint64_t)t.r_pad, 32, (uint32_t)p.prow, true) ||
         !cached_map_plain_2d(&mapL, L, 4, (uint64_t)R, (uint64_t)(B * B), (uint64_t)R, (uint32_t)t.w,
                              (uint32_t)(B * B)) ||
         !cached_map_plain_2d(&mapU, u, 4, (uint64_t)R, (uint64_t)(N * B), (uint64_t)R, (uint32_t)t.w,
