@@ -470,6 +470,7 @@ struct UpParams {
   uint16_t* m;
   WsHeader* hdr;
   int32_t rows, H, chunks, htiles, stages;
+  int32_t arow;  // rows per ub box: 128, or a lone M tile's rows rounded up to 8
   const uint32_t* skip;  // nullable: see pass_skipped
 };
 
@@ -484,6 +485,7 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
   if (threadIdx.x == 0) XP_TRACE_MARK(16);
   uint8_t* smem = align1024(smem_raw);
   constexpr uint32_t stage_bytes = LT_A_CHUNK + 2 * LT_BOX;  // 32 KB
+  const uint32_t stage_tx = (uint32_t)p.arow * 128u + 2 * LT_BOX;  // bytes a stage's copies bring
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)p.stages * stage_bytes);
   uint64_t* empty = full + p.stages;
   uint64_t* acc_full = empty + p.stages;
@@ -527,7 +529,7 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
     issued = pre;
     for (int i = 0; i < pre; ++i) {
       uint8_t* dst = smem + (size_t)i * stage_bytes;
-      if (lane == 0) mbar_arrive_expect_tx(&full[i], stage_bytes);
+      if (lane == 0) mbar_arrive_expect_tx(&full[i], stage_tx);
       __syncwarp();
       if (lane == 1) tma_load_2d_hint(dst + LT_A_CHUNK, &mapWg, ht * 64, i * LT_BK, &full[i], pol);
       if (lane == 2) tma_load_2d_hint(dst + LT_A_CHUNK + LT_BOX, &mapWu, ht * 64, i * LT_BK, &full[i], pol);
@@ -542,7 +544,7 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
       int ok = 1;
       if (lane == 0) {
         if (k >= 1 && !mbar_wait(&empty[s], (k - 1) & 1)) ok = 0;
-        else mbar_arrive_expect_tx(&full[s], stage_bytes);
+        else mbar_arrive_expect_tx(&full[s], stage_tx);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
@@ -650,6 +652,7 @@ struct DownParams {
   uint16_t* lat;
   WsHeader* hdr;
   int32_t N, B, R, tn, S, w, chunks, ntiles, stages;
+  int32_t arow;  // rows per m / residual box: 128, or a lone M tile's rows rounded up to 8
   uint32_t region, bar_off;
   const uint32_t* skip;  // nullable: see pass_skipped
 };
@@ -666,6 +669,7 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
   uint8_t* smem = align1024(smem_raw);
   const uint32_t b_bytes = (uint32_t)p.tn * LT_BK * 2;
   const uint32_t stage_bytes = LT_A_CHUNK + b_bytes;
+  const uint32_t stage_tx = (uint32_t)p.arow * 128u + b_bytes;  // bytes a stage's copies bring
   const int ld = p.tn + 4;  // floats per row of red (a 16-byte multiple)
   const float* us = reinterpret_cast<const float*>(smem + p.region);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
@@ -721,7 +725,7 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
     issued = pre;
     for (int i = 0; i < pre; ++i) {
       uint8_t* dst = smem + (size_t)i * stage_bytes;
-      if (lane == 0) mbar_arrive_expect_tx(&full[i], stage_bytes);
+      if (lane == 0) mbar_arrive_expect_tx(&full[i], stage_tx);
       __syncwarp();
       if (lane >= 1 && lane <= p.tn / 64)
         tma_load_2d_hint(dst + LT_A_CHUNK + (lane - 1) * LT_BOX, &mapWd, nt * p.tn + (lane - 1) * 64, (c0 + i) * LT_BK,
@@ -734,7 +738,7 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
     if (lane < pre)
       tma_load_2d(smem + (size_t)lane * stage_bytes, &mapM, (c0 + lane) * LT_BK, mt * LT_BM, &full[lane]);
     if (lane == 31) {
-      mbar_arrive_expect_tx(aux_full, (uint32_t)(LT_BM * p.w * 4));
+      mbar_arrive_expect_tx(aux_full, (uint32_t)(p.arow * p.w * 4));
       tma_load_2d(smem + p.region, &mapU, col0, mt * LT_BM, aux_full);
     }
     for (int i = pre; i < nck; ++i) {
@@ -742,7 +746,7 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
       int ok = 1;
       if (lane == 0) {
         if (k >= 1 && !mbar_wait(&empty[s], (k - 1) & 1)) ok = 0;
-        else mbar_arrive_expect_tx(&full[s], stage_bytes);
+        else mbar_arrive_expect_tx(&full[s], stage_tx);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
@@ -1026,13 +1030,14 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     p.chunks = (int32_t)((R + LT_BK - 1) / LT_BK);
     p.htiles = (int32_t)(H / 64);
     const int mtiles = (rows + LT_BM - 1) / LT_BM;
+    p.arow = rows < LT_BM ? (rows + 7) / 8 * 8 : LT_BM;  // a lone partial M tile copies only its rows
     p.stages = p.chunks < 6 ? (p.chunks < 2 ? 2 : p.chunks) : 6;
     // more CTAs than SMs: a three-stage ring, so two CTAs fit on an SM and
     // the grid runs in one wave
     if ((int64_t)mtiles * p.htiles > g_lt_sms[dev] && p.stages > 3) p.stages = 3;
     const size_t smem = 1024 + (size_t)p.stages * (LT_A_CHUNK + 2 * LT_BOX) + 8 * (2 * p.stages + 1) + 16;
     CUtensorMap mapUb, mapWg, mapWu;
-    if (!cached_map_bf16_2d(&mapUb, ub, (uint64_t)R, (uint64_t)rows, (uint64_t)R, LT_BK, LT_BM) ||
+    if (!cached_map_bf16_2d(&mapUb, ub, (uint64_t)R, (uint64_t)rows, (uint64_t)R, LT_BK, (uint32_t)p.arow) ||
         !cached_map_bf16_2d(&mapWg, Wg, (uint64_t)H, (uint64_t)R, (uint64_t)H, 64, LT_BK) ||
         !cached_map_bf16_2d(&mapWu, Wu, (uint64_t)H, (uint64_t)R, (uint64_t)H, 64, LT_BK))
       return XP_ERR_LAUNCH;
@@ -1072,6 +1077,7 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     auto total = [&](int st) { return 1024 + region_of(st) + us_bytes + 8 * (2 * st + 2) + 16; };
     const int per_cta = (p.chunks + p.S - 1) / p.S;
     const int mtiles = (rows + LT_BM - 1) / LT_BM;
+    p.arow = rows < LT_BM ? (rows + 7) / 8 * 8 : LT_BM;  // a lone partial M tile copies only its rows
     p.stages = per_cta < 6 ? (per_cta < 2 ? 2 : per_cta) : 6;
     // more CTAs than SMs: a four-stage ring, so two CTAs fit on an SM and the
     // grid runs in one wave
@@ -1080,9 +1086,9 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     p.bar_off = p.region + (uint32_t)us_bytes;
     const size_t smem = total(p.stages);
     CUtensorMap mapM, mapWd, mapU;
-    if (!cached_map_bf16_2d(&mapM, m, (uint64_t)H, (uint64_t)rows, (uint64_t)H, LT_BK, LT_BM) ||
+    if (!cached_map_bf16_2d(&mapM, m, (uint64_t)H, (uint64_t)rows, (uint64_t)H, LT_BK, (uint32_t)p.arow) ||
         !cached_map_bf16_2d(&mapWd, Wd, (uint64_t)R, (uint64_t)H, (uint64_t)R, 64, LT_BK) ||
-        !cached_map_plain_2d(&mapU, u, 4, (uint64_t)R, (uint64_t)rows, (uint64_t)R, (uint32_t)p.w, LT_BM))
+        !cached_map_plain_2d(&mapU, u, 4, (uint64_t)R, (uint64_t)rows, (uint64_t)R, (uint32_t)p.w, (uint32_t)p.arow))
       return XP_ERR_LAUNCH;
     void* args[] = {&mapM, &mapWd, &mapU, &p};
     const void* down_fn = do_mlp ? (const void*)mlp_down_kernel<false> : (const void*)mlp_down_kernel<true>;

@@ -82,6 +82,9 @@ constexpr uint32_t RO_TMEM_ACC = 256;                  // accumulators: [256, 38
 struct ReadoutParams {
   const uint16_t* lat;
   int32_t rows, V, R, kch, mp, nt, per, B;  // kch = ceil(R / 64) K chunks (boxes) per tile
+  // rows per latent / base box: 128, or the rows of a lone partial M tile
+  // rounded up to 8 (fewer rows copied; the rest of the box is never read out)
+  int32_t box_rows;
   int64_t* blk;
   int32_t* changed;
   unsigned long long* keys;
@@ -260,12 +263,16 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
     const int rounds = (p.kch + RO_A_ROUND - 1) / RO_A_ROUND;
     bool a_dead = false;
     const uint64_t pol_base = policy_evict_first();  // read once per pass
+    // an M tile with no rows (the second tile of a lone pair) copies nothing:
+    // its barriers complete on the arrival alone
+    const bool live = m_tile * RO_BM < p.rows;
+    const uint32_t box_bytes = live ? (uint32_t)p.box_rows * 128u : 0u;
     if (lane == 0) {
       prefetch_tensormap(&mapLat);
       prefetch_tensormap(&mapBase);
     }
     // the first base tiles into L2 while the latent is still being computed
-    if (lane < 2 * RO_NBASE && lane / 2 < ntiles)
+    if (live && lane < 2 * RO_NBASE && lane / 2 < ntiles)
       tma_prefetch_2d(&mapBase, (n_begin + lane / 2) * RO_BN + (lane & 1) * 64, m_tile * RO_BM);
     pdl_wait();
     for (int r = 0; r < rounds && !a_dead; ++r) {
@@ -273,13 +280,13 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       int ok = 1;
       if (lane == 0) {
         if (r >= 1 && !mbar_wait(a_free, (r - 1) & 1)) ok = 0;
-        else mbar_arrive_expect_tx(&a_full[r], (uint32_t)nbox * RO_BASE_BOX);
+        else mbar_arrive_expect_tx(&a_full[r], (uint32_t)nbox * box_bytes);
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) {
         a_dead = true;
         break;
       }
-      if (lane < nbox)
+      if (live && lane < nbox)
         tma_load_2d(a_box(lane), &mapLat, (RO_A_ROUND * r + lane) * 64, m_tile * RO_BM, &a_full[r]);
       lat_issued = r + 1;
     }
@@ -298,7 +305,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
         int ok = 1;
         if (lane == 0) {
           if (k >= 1 && !mbar_wait(&base_empty[bb], (k - 1) & 1)) ok = 0;
-          else mbar_arrive_expect_tx(&base_full[bb], RO_BASE_TILE);
+          else mbar_arrive_expect_tx(&base_full[bb], 2u * box_bytes);
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
           timed_out = 1;
@@ -306,7 +313,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
           break;
         }
         base_issued = t + 1;
-        if (lane < 2)
+        if (live && lane < 2)
           tma_load_2d_hint(sBase + (size_t)bb * RO_BASE_TILE + lane * RO_BASE_BOX, &mapBase, n0 + lane * 64,
                            m_tile * RO_BM, &base_full[bb], pol_base);
       }
@@ -378,7 +385,7 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
           timed_out = 1;
           flag_error(p.hdr, XP_DEVERR_TIMEOUT);
         }
-        if (ok) {
+        if (ok && m_tile * RO_BM < p.rows) {  // an M tile with no rows leaves its A alone
 #pragma unroll
           for (int j = 0; j < RO_A_ROUND / 2; ++j) {
             const int box = 2 * j + h, kc = RO_A_ROUND * r + box;
@@ -593,9 +600,13 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
   CUtensorMap mapW2, mapBase, mapLat;
   if (!cached_map_bf16_2d(&mapW2, W2t, (uint64_t)R, (uint64_t)V, (uint64_t)R, 64, RO_HALF)) return XP_ERR_LAUNCH;
   // base: columns past V read as NaN (see ro_chunk)
-  if (!cached_map_bf16_2d(&mapBase, base, (uint64_t)V, (uint64_t)rows, (uint64_t)ld_base, 64, RO_BM, true))
+  // a lone partial M tile (rows < 128) copies only its rows, rounded up to 8
+  const int32_t box_rows = rows < RO_BM ? (int32_t)((rows + 7) / 8 * 8) : RO_BM;
+  if (!cached_map_bf16_2d(&mapBase, base, (uint64_t)V, (uint64_t)rows, (uint64_t)ld_base, 64, (uint32_t)box_rows,
+                          true))
     return XP_ERR_LAUNCH;
-  if (!cached_map_bf16_2d(&mapLat, lat, (uint64_t)R, (uint64_t)rows, (uint64_t)R, 64, RO_BM)) return XP_ERR_LAUNCH;
+  if (!cached_map_bf16_2d(&mapLat, lat, (uint64_t)R, (uint64_t)rows, (uint64_t)R, 64, (uint32_t)box_rows))
+    return XP_ERR_LAUNCH;
 
   ReadoutParams p;
   ArgmaxWs w = argmax_ws(ws, rows);
@@ -605,6 +616,7 @@ xp_status launch_readout_argmax(const uint16_t* lat, const uint16_t* W2t, const 
   p.V = (int32_t)V;
   p.R = (int32_t)R;
   p.kch = kch;  // A staged in TMEM up to the last K chunk, zero beyond R
+  p.box_rows = box_rows;
   p.mp = sp.mp;
   p.nt = sp.nt;
   p.per = sp.per;
