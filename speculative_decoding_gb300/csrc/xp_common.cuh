@@ -116,6 +116,7 @@ __host__ inline ArgmaxWs argmax_ws(void* ws, int64_t rows) {
 // then sum in a fixed order.
 struct ProjTiling {
   int32_t bpt, mtiles, tn, ntiles, chunks, S, w;
+  int32_t lw;  // mixer-weight columns held at once: w, or w/2 (two rounds) when w columns do not fit
   int64_t rows_pad, r_pad;  // partial-sum buffer: [S][rows_pad][r_pad] fp32
 };
 
@@ -126,8 +127,8 @@ struct ProjTiling {
 // whose place the mixer's output (u fp32 and bf16(u), w columns) takes later:
 // the larger of the two.  Then the mixer weights of the w columns (the whole
 // [B][B] square), the hidden cache of those columns, the token table, and the
-// barriers (full/empty per stage, acc_full, aux_full, slice_full) and the TMEM
-// address slot; 1024 bytes of alignment slack in front.
+// barriers (full/empty per stage, acc_full, aux_full, slice_full, ls_full) and
+// the TMEM address slot; 1024 bytes of alignment slack in front.
 struct ProjSmem {
   uint32_t region, hc_off, tok_off, bar_off;
   size_t total;
@@ -137,7 +138,7 @@ __host__ inline ProjSmem proj_smem(const ProjTiling& t, int64_t B, int stages) {
   const size_t stage_bytes = rows * 64 * 2 + (size_t)t.tn * 64 * 2;
   const size_t pst = rows * (size_t)(t.tn * 4 > t.w * 6 ? t.tn * 4 : t.w * 6);
   const size_t sl_xs = (((size_t)(t.S + 1) * rows * t.w * 4 + 1023) & ~size_t(1023)) + pst;
-  const size_t ls = ((size_t)(B * B * t.w * 4) + 127) & ~size_t(127);
+  const size_t ls = ((size_t)(B * B * t.lw * 4) + 127) & ~size_t(127);
   const size_t hc = (rows * t.w * 2 + 127) & ~size_t(127);
   const size_t ring = (size_t)stages * stage_bytes;
   ProjSmem m;
@@ -145,7 +146,7 @@ __host__ inline ProjSmem proj_smem(const ProjTiling& t, int64_t B, int stages) {
   m.hc_off = m.region + (uint32_t)ls;
   m.tok_off = m.hc_off + (uint32_t)hc;
   m.bar_off = m.tok_off + 8 * (uint32_t)rows;
-  m.total = 1024 + (size_t)m.bar_off + 8 * (2 * (size_t)stages + 3) + 16;
+  m.total = 1024 + (size_t)m.bar_off + 8 * (2 * (size_t)stages + 4) + 16;
   return m;
 }
 // Dynamic shared memory a latent-stage kernel may use: the 227 KB opt-in
@@ -167,12 +168,18 @@ __host__ inline ProjTiling proj_tiling(int64_t N, int64_t B, int64_t D, int64_t 
          (int64_t)t.mtiles * t.ntiles * t.S * 2 <= 128)
     t.S *= 2;
   t.w = t.tn / t.S;
-  // fewer slices while a CTA's share of the epilogue (w columns of mixer
-  // weights, partial slices and mixer tiles) does not fit beside a two-stage
-  // ring
+  t.lw = t.w;
+  // while a CTA's share of the epilogue (partial slices, mixer tiles and
+  // mixer weights) does not fit beside a two-stage ring: first hold the mixer
+  // weights of half the columns at a time, then take fewer slices
   while (t.S > 1 && proj_smem(t, B, 2).total > kLatentSmemBudget) {
+    if (t.lw == t.w && t.w >= 16) {
+      t.lw = t.w / 2;
+      continue;
+    }
     t.S /= 2;
     t.w = t.tn / t.S;
+    t.lw = t.w;
   }
   // with the D sum unsplit (many output tiles) a CTA mixes all its tile's
   // channels: 64-channel tiles keep its shared memory (the mixer weights
@@ -181,6 +188,7 @@ __host__ inline ProjTiling proj_tiling(int64_t N, int64_t B, int64_t D, int64_t 
     t.tn = 64;
     t.ntiles = (int32_t)((R + t.tn - 1) / t.tn);
     t.w = t.tn;
+    t.lw = t.w;
   }
   t.rows_pad = (int64_t)t.mtiles * 128;
   t.r_pad = (int64_t)t.ntiles * t.tn;

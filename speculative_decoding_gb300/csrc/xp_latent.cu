@@ -78,7 +78,7 @@ struct ProjParams {
   float* part;
   uint32_t* cnt;
   WsHeader* hdr;
-  int32_t N, B, V, D, R, bpt, tn, S, w, chunks, ntiles, stages;
+  int32_t N, B, V, D, R, bpt, tn, S, w, lw, chunks, ntiles, stages;
   int32_t prow;  // rows of a partial tile that are stored and summed (128, or fewer for a lone M tile)
   int64_t rows_pad, r_pad;
   uint32_t region, hc_off, tok_off, bar_off;
@@ -86,6 +86,8 @@ struct ProjParams {
 };
 
 
+// kHalfL: the mixer weights of half the CTA's columns at a time (lw = w / 2)
+template <bool kHalfL>
 __global__ void __launch_bounds__(LT_THREADS, 1)
 proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_constant__ CUtensorMap mapHc,
                 const __grid_constant__ CUtensorMap mapPart, const __grid_constant__ CUtensorMap mapPartSt,
@@ -111,7 +113,8 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
   uint64_t* acc_full = empty + p.stages;
   uint64_t* aux_full = acc_full + 1;    // Ls and hcs landed
   uint64_t* slice_full = aux_full + 1;  // the S partial slices landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(slice_full + 1);
+  uint64_t* ls_full = slice_full + 1;   // the second round of mixer weights landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ls_full + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ks = (int)(blockIdx.x % p.S);
@@ -135,6 +138,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     mbar_init(acc_full, 1);
     mbar_init(aux_full, 1);
     mbar_init(slice_full, 1);
+    mbar_init(ls_full, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -149,7 +153,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
   pdl_launch_dependents();
   // copies requested, for the drain before exit after a timed-out wait
   int timed_out = 0, issued = 0;
-  bool aux_issued = false, slices_issued = false;
+  bool aux_issued = false, slices_issued = false, ls_issued = false;
 
   if (warp == 0) {
     // Nothing this warp reads is written by the preceding kernels, so it
@@ -164,7 +168,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     // (the whole [B][B] square of L for these w channels)
     auto aux_copies = [&]() {
       aux_issued = true;
-      if (lane == 0) mbar_arrive_expect_tx(aux_full, (uint32_t)(p.B * p.B * p.w * 4) + (uint32_t)(LT_BM * p.w * 2));
+      if (lane == 0) mbar_arrive_expect_tx(aux_full, (uint32_t)(p.B * p.B * p.lw * 4) + (uint32_t)(LT_BM * p.w * 2));
       __syncwarp();
       if (lane == 0) tma_load_2d(smem + p.hc_off, &mapHc, col0, mt * p.bpt * p.B, aux_full);
       if (lane == 1) tma_load_2d(Ls, &mapL, col0, 0, aux_full);
@@ -402,37 +406,60 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     // past R are clipped by the stores)
     float* us = reinterpret_cast<float*>(pst);                            // [bpt*B][w]
     uint16_t* ubs = reinterpret_cast<uint16_t*>(pst + (size_t)LT_BM * p.w * 4);  // [bpt*B][w]
-    if (nbl * p.w <= 16) {
-      // very few (block, channel) pairs (one block, a narrow slice): one
-      // output per thread, the same sum in the same order as below
-      for (int it = et; it < nbl * p.B * p.w; it += 128) {
-        const int bb = it / p.w, c = it - bb * p.w;  // bb = bl * B + b
-        const int bl = bb / p.B, b = bb - bl * p.B;
-        const float* Lb = Ls + (b * p.B) * p.w + c;
-        const float* xc = xs + (bl * p.B) * p.w + c;
-        float uu = 0.f;
-        for (int j = 0; j <= b; ++j) uu = fmaf(Lb[j * p.w], xc[j * p.w], uu);
-        const int o = bb * p.w + c;
-        us[o] = uu;
-        ubs[o] = (uint16_t)(f32x2_to_bf16x2(uu, 0.f) & 0xffffu);
-      }
-    } else for (int it = et; it < nbl * p.w; it += 128) {
-      const int bl = it / p.w, c = it - bl * p.w;
-      float x[LT_MAX_B];
-#pragma unroll
-      for (int j = 0; j < LT_MAX_B; ++j) x[j] = j < p.B ? xs[(bl * p.B + j) * p.w + c] : 0.f;
-#pragma unroll
-      for (int b = 0; b < LT_MAX_B; ++b) {
-        if (b < p.B) {
+    // the mixer on columns [cb, cb + lw) with Ls holding their weights
+    auto mix = [&](const int cb, const int lw) {
+      if (nbl * lw <= 16) {
+        // very few (block, channel) pairs (one block, a narrow slice): one
+        // output per thread, the same sum in the same order as below
+        for (int it = et; it < nbl * p.B * lw; it += 128) {
+          const int bb = it / lw, cl = it - bb * lw;  // bb = bl * B + b
+          const int bl = bb / p.B, b = bb - bl * p.B, c = cb + cl;
+          const float* Lb = Ls + (b * p.B) * lw + cl;
+          const float* xc = xs + (bl * p.B) * p.w + c;
           float uu = 0.f;
-          const float* Lb = Ls + (b * p.B) * p.w + c;
-#pragma unroll
-          for (int j = 0; j <= b; ++j) uu = fmaf(Lb[j * p.w], x[j], uu);
-          const int o = (bl * p.B + b) * p.w + c;
+          for (int j = 0; j <= b; ++j) uu = fmaf(Lb[j * lw], xc[j * p.w], uu);
+          const int o = bb * p.w + c;
           us[o] = uu;
           ubs[o] = (uint16_t)(f32x2_to_bf16x2(uu, 0.f) & 0xffffu);
         }
+      } else {
+        for (int it = et; it < nbl * lw; it += 128) {
+          const int bl = it / lw, cl = it - bl * lw, c = cb + cl;
+          float x[LT_MAX_B];
+#pragma unroll
+          for (int j = 0; j < LT_MAX_B; ++j) x[j] = j < p.B ? xs[(bl * p.B + j) * p.w + c] : 0.f;
+#pragma unroll
+          for (int b = 0; b < LT_MAX_B; ++b) {
+            if (b < p.B) {
+              float uu = 0.f;
+              const float* Lb = Ls + (b * p.B) * lw + cl;
+#pragma unroll
+              for (int j = 0; j <= b; ++j) uu = fmaf(Lb[j * lw], x[j], uu);
+              const int o = (bl * p.B + b) * p.w + c;
+              us[o] = uu;
+              ubs[o] = (uint16_t)(f32x2_to_bf16x2(uu, 0.f) & 0xffffu);
+            }
+          }
+        }
       }
+    };
+    if constexpr (!kHalfL) {
+      mix(0, p.w);
+    } else {
+      // Ls holds the weights of half the columns: the second half's are
+      // copied in once every thread is done with the first's
+      mix(0, p.lw);
+      named_barrier_sync(1, 128);
+      if (et == 0) {
+        mbar_arrive_expect_tx(ls_full, (uint32_t)(p.B * p.B * p.lw * 4));
+        tma_load_2d(Ls, &mapL, col0 + p.lw, 0, ls_full);
+        ls_issued = true;
+      }
+      if (!timed_out && !mbar_wait(ls_full, 0)) {
+        timed_out = 1;
+        flag_error(p.hdr, XP_DEVERR_TIMEOUT);
+      }
+      mix(p.lw, p.lw);
     }
     fence_proxy_async_smem();
     named_barrier_sync(1, 128);
@@ -454,6 +481,9 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
       (void)mbar_wait(&full[j % p.stages], (uint32_t)(j / p.stages) & 1);
     if (aux_issued) (void)mbar_wait(aux_full, 0);
     if (slices_issued) (void)mbar_wait(slice_full, 0);
+  }
+  if constexpr (kHalfL) {
+    if (threadIdx.x == 64 && ls_issued) (void)mbar_wait(ls_full, 0);  // landed before exit (done on the normal path)
   }
   __syncthreads();
   if (threadIdx.x == 0) XP_TRACE_MARK(14);
@@ -942,7 +972,8 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
                                   max_smem - (int)fa.sharedSizeBytes) == cudaSuccess &&
              cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
     };
-    if (!allow((const void*)proj_mix_kernel) || !allow((const void*)mlp_up_kernel<false>) ||
+    if (!allow((const void*)proj_mix_kernel<false>) || !allow((const void*)proj_mix_kernel<true>) ||
+        !allow((const void*)mlp_up_kernel<false>) ||
         !allow((const void*)mlp_up_kernel<true>) || !allow((const void*)mlp_down_kernel<false>) ||
         !allow((const void*)mlp_down_kernel<true>))
       return XP_ERR_LAUNCH;
@@ -980,6 +1011,7 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
     p.chunks = t.chunks;
     p.S = t.S;
     p.w = t.w;
+    p.lw = t.lw;
     p.ntiles = t.ntiles;
     p.rows_pad = t.rows_pad;
     p.r_pad = t.r_pad;
@@ -1005,7 +1037,7 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
                              (uint32_t)t.w, (uint32_t)p.prow) ||
         !cached_map_plain_2d(&mapPartSt, p.part, 4, (uint64_t)t.r_pad, (uint64_t)(t.S * t.rows_pad),
                              (uint64_t)t.r_pad, 32, (uint32_t)p.prow, true) ||
-        !cached_map_plain_2d(&mapL, L, 4, (uint64_t)R, (uint64_t)(B * B), (uint64_t)R, (uint32_t)t.w,
+        !cached_map_plain_2d(&mapL, L, 4, (uint64_t)R, (uint64_t)(B * B), (uint64_t)R, (uint32_t)t.lw,
                              (uint32_t)(B * B)) ||
         !cached_map_plain_2d(&mapU, u, 4, (uint64_t)R, (uint64_t)(N * B), (uint64_t)R, (uint32_t)t.w,
                              (uint32_t)(t.bpt * B)) ||
@@ -1013,7 +1045,8 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
                              (uint32_t)(t.bpt * B)))
       return XP_ERR_LAUNCH;
     void* args[] = {&mapWlat, &mapHc, &mapPart, &mapPartSt, &mapL, &mapU, &mapUbS, &p};
-    if (launch_ex((const void*)proj_mix_kernel, dim3((unsigned)(t.mtiles * t.ntiles * t.S)), smem, stream, 1, args) !=
+    const void* pm_fn = t.lw == t.w ? (const void*)proj_mix_kernel<false> : (const void*)proj_mix_kernel<true>;
+    if (launch_ex(pm_fn, dim3((unsigned)(t.mtiles * t.ntiles * t.S)), smem, stream, 1, args) !=
         cudaSuccess) {
       (void)cudaGetLastError();  // a failed launch must not be reported again by a later call
       return XP_ERR_LAUNCH;
