@@ -43,8 +43,12 @@ constexpr uint32_t LT_BOX = 64 * 64 * 2;            // one 64 x 64 bf16 box (8 K
 constexpr int LT_MAX_B = 16;
 constexpr int LT_MAX_S = 8;
 
+// The dynamic shared-memory base rounded up to 1024 bytes, as an offset from
+// the base pointer itself (not a round trip through an integer), so the
+// compiler keeps knowing that the result points into shared memory and emits
+// shared-memory loads and stores for every pointer derived from it.
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+  return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
 }
 
 // bf16 bits -> float
@@ -376,6 +380,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
       timed_out = 1;
       flag_error(p.hdr, XP_DEVERR_TIMEOUT);
     }
+    if (et == 127) XP_TRACE_MARK(28);
     // ---- epilogue 2: x = hcache + sum of the S partials (slice order) for
     // this CTA's columns of all rows, four columns per item
     const int wq = p.w / 4, items = LT_BM * wq;
@@ -461,9 +466,11 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
       }
       mix(p.lw, p.lw);
     }
+    if (et == 127) XP_TRACE_MARK(29);
     fence_proxy_async_smem();
     named_barrier_sync(1, 128);
     if (et == 0) {
+      XP_TRACE_MARK(30);
       tma_store_2d(&mapU, us, col0, mt * p.bpt * p.B);
       tma_store_2d(&mapUb, ubs, col0, mt * p.bpt * p.B);
       bulk_commit();

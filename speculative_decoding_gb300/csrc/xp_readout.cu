@@ -133,7 +133,9 @@ __global__ void __launch_bounds__(RO_THREADS, 1)
 readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ CUtensorMap mapBase,
                       const __grid_constant__ CUtensorMap mapLat, const ReadoutParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // rounded up to 1024 bytes as an offset from smem_raw, so the compiler
+  // keeps the shared address space for every pointer derived from it
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sB = smem;                                                  // RO_SLOTS x 64 KB
   uint8_t* sBase = smem + (size_t)RO_SLOTS * RO_W2_SLOT;                // RO_NBASE x 32 KB
   uint64_t* bars = reinterpret_cast<uint64_t*>(sBase + (size_t)RO_NBASE * RO_BASE_TILE);
