@@ -383,10 +383,13 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     if (et == 127) XP_TRACE_MARK(28);
     // ---- epilogue 2: x = hcache + sum of the S partials (slice order) for
     // this CTA's columns of all rows, four columns per item
-    const int wq = p.w / 4, items = LT_BM * wq;
+    // w is a power of two (a power-of-two split of 64 or 128 channels): the
+    // item index splits by shifts, and the tile's rows that hold blocks are
+    // the first nbl * B
+    const int wq = p.w / 4, items = LT_BM * wq, wq_sh = __ffs(wq) - 1, live_rows = nbl * p.B;
     for (int it = et; it < items; it += 128) {
-      const int rr = it / wq, gg = it - rr * wq;
-      if (rr / p.B >= nbl) continue;
+      const int rr = it >> wq_sh, gg = it & (wq - 1);
+      if (rr >= live_rows) continue;
       float4 a = *reinterpret_cast<const float4*>(slices + rr * p.w + 4 * gg);
       for (int q = 1; q < p.S; ++q) {
         const float4 v = *reinterpret_cast<const float4*>(slices + ((size_t)q * LT_BM + rr) * p.w + 4 * gg);
@@ -428,8 +431,9 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
           ubs[o] = (uint16_t)(f32x2_to_bf16x2(uu, 0.f) & 0xffffu);
         }
       } else {
+        const int lw_sh = __ffs(lw) - 1;  // lw is a power of two
         for (int it = et; it < nbl * lw; it += 128) {
-          const int bl = it / lw, cl = it - bl * lw, c = cb + cl;
+          const int bl = it >> lw_sh, cl = it & (lw - 1), c = cb + cl;
           float x[LT_MAX_B];
 #pragma unroll
           for (int j = 0; j < LT_MAX_B; ++j) x[j] = j < p.B ? xs[(bl * p.B + j) * p.w + c] : 0.f;
