@@ -568,12 +568,16 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
     const uint64_t pol = policy_evict_last();  // every pass re-reads Wg, Wu
     const int pre = p.chunks < p.stages ? p.chunks : p.stages;
     issued = pre;
-    for (int i = 0; i < pre; ++i) {
-      uint8_t* dst = smem + (size_t)i * stage_bytes;
-      if (lane == 0) mbar_arrive_expect_tx(&full[i], stage_tx);
-      __syncwarp();
-      if (lane == 1) tma_load_2d_hint(dst + LT_A_CHUNK, &mapWg, ht * 64, i * LT_BK, &full[i], pol);
-      if (lane == 2) tma_load_2d_hint(dst + LT_A_CHUNK + LT_BOX, &mapWu, ht * 64, i * LT_BK, &full[i], pol);
+    // the first stages armed, then their Wg and Wu boxes one lane each (a
+    // thread issues tiled copies one after another, ~0.27 us apiece, so one
+    // lane per box keeps this ahead of the dependency wait short)
+    if (lane == 0)
+      for (int i = 0; i < pre; ++i) mbar_arrive_expect_tx(&full[i], stage_tx);
+    __syncwarp();
+    if (lane < 2 * pre) {
+      const int i = lane >> 1;
+      uint8_t* dst = smem + (size_t)i * stage_bytes + LT_A_CHUNK + (lane & 1) * LT_BOX;
+      tma_load_2d_hint(dst, (lane & 1) ? &mapWu : &mapWg, ht * 64, i * LT_BK, &full[i], pol);
     }
     pdl_wait();
     if (lane == 0) XP_TRACE_MARK(18);
@@ -764,13 +768,15 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
     const uint64_t pol = policy_evict_last();  // every pass re-reads Wd
     const int pre = nck < p.stages ? nck : p.stages;
     issued = pre;
-    for (int i = 0; i < pre; ++i) {
-      uint8_t* dst = smem + (size_t)i * stage_bytes;
-      if (lane == 0) mbar_arrive_expect_tx(&full[i], stage_tx);
-      __syncwarp();
-      if (lane >= 1 && lane <= p.tn / 64)
-        tma_load_2d_hint(dst + LT_A_CHUNK + (lane - 1) * LT_BOX, &mapWd, nt * p.tn + (lane - 1) * 64, (c0 + i) * LT_BK,
-                         &full[i], pol);
+    // the first stages armed, then their Wd boxes one lane each (see mlp_up)
+    if (lane == 0)
+      for (int i = 0; i < pre; ++i) mbar_arrive_expect_tx(&full[i], stage_tx);
+    __syncwarp();
+    const int bpb = p.tn / 64;  // Wd boxes per stage
+    if (lane < pre * bpb) {
+      const int i = lane / bpb, bx = lane - i * bpb;
+      tma_load_2d_hint(smem + (size_t)i * stage_bytes + LT_A_CHUNK + bx * LT_BOX, &mapWd, nt * p.tn + bx * 64,
+                       (c0 + i) * LT_BK, &full[i], pol);
     }
     pdl_wait();
     if (lane == 0) XP_TRACE_MARK(34);
