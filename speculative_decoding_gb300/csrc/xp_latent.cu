@@ -323,13 +323,15 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     }
     fence_proxy_async_smem();
     named_barrier_sync(1, 128);
-    if (threadIdx.x == 64) {
-      for (int c = 0; c < p.tn / 32; ++c)
-        tma_store_2d(&mapPartSt, pst + (size_t)c * (LT_BM * 128), nt * p.tn + c * 32,
-                     (int)((int64_t)ks * p.rows_pad + (int64_t)mt * LT_BM));
+    // one 32-column box per thread (a thread issues tiled copies ~0.27 us
+    // apart), each waited for by the thread that issued it
+    const int c = threadIdx.x - 64;
+    if (c < p.tn / 32) {
+      tma_store_2d(&mapPartSt, pst + (size_t)c * (LT_BM * 128), nt * p.tn + c * 32,
+                   (int)((int64_t)ks * p.rows_pad + (int64_t)mt * LT_BM));
       bulk_commit();
-      bulk_wait_all();  // the partial tile is in global memory
-      XP_TRACE_MARK(10);
+      bulk_wait_all();  // this box of the partial tile is in global memory
+      if (c == 0) XP_TRACE_MARK(10);
     }
   }
   tc_fence_before();
@@ -473,13 +475,13 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     if (et == 127) XP_TRACE_MARK(29);
     fence_proxy_async_smem();
     named_barrier_sync(1, 128);
-    if (et == 0) {
-      XP_TRACE_MARK(30);
-      tma_store_2d(&mapU, us, col0, mt * p.bpt * p.B);
-      tma_store_2d(&mapUb, ubs, col0, mt * p.bpt * p.B);
+    if (et < 2) {  // u and bf16(u), one thread each
+      if (et == 0) XP_TRACE_MARK(30);
+      if (et == 0) tma_store_2d(&mapU, us, col0, mt * p.bpt * p.B);
+      else tma_store_2d(&mapUb, ubs, col0, mt * p.bpt * p.B);
       bulk_commit();
       bulk_wait_all();
-      XP_TRACE_MARK(13);
+      if (et == 0) XP_TRACE_MARK(13);
     }
   }
   tc_fence_before();
