@@ -125,11 +125,12 @@ add_argmax_kernel(const uint16_t* __restrict__ base, int64_t ld_base, const uint
   }
 }
 
-// 128 threads x 8 vectors of 8 elements: 8192 columns per CTA (measured
-// against 256 x 4, 256 x 8, 512 x 4 and 512 x 2 at 480 x 152064: 45.3 /
-// 45.6 / 46.5 / 51.5 / 55.3 us)
-constexpr int AA_THREADS = 128;
-constexpr int AA_VEC = 8;
+// 256 threads x 4 vectors of 8 elements: 8192 columns per CTA.  Back to back
+// at 480 x 152064, 128 x 8 / 256 x 4 / 256 x 8 / 512 x 4 / 512 x 2 measured
+// 45.3 / 45.6 / 46.5 / 51.5 / 55.3 us, but a single cold launch (ncu) took
+// 48.9 us with 128 x 8 against 47.0 with 256 x 4
+constexpr int AA_THREADS = 256;
+constexpr int AA_VEC = 4;
 
 xp_status launch_add_argmax(const uint16_t* base, int64_t ld_base, const uint16_t* bias, int64_t ld_bias,
                             int64_t rows, int64_t V, int64_t* blk, int64_t B, void* ws,
