@@ -210,23 +210,29 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(LT_BM, p.tn, 0, 1);
       bool dead = false;
+      // stage 0's descriptors; a stage adds its offset and a K step of 16
+      // adds 32 bytes to A and 16 rows (2 KB) to B (address field: 16-byte units)
+      const uint64_t adesc0 = smem_desc_sw128(smem_u32(smem), 16, 1024);
+      const uint64_t bdesc0 = smem_desc_sw128(smem_u32(smem) + LT_A_CHUNK, LT_BOX, 1024);
+      uint32_t s = 0, ph = 0, soff = 0;
       for (int i = 0; i < nck; ++i) {
-        const uint32_t s = i % p.stages, k = i / p.stages;
-        if (!mbar_wait(&full[s], k & 1)) {
+        if (!mbar_wait(&full[s], ph)) {
           dead = true;
           break;
         }
         tc_fence_after();
         if (i == 0) XP_TRACE_MARK(7);
-        const uint32_t a_base = smem_u32(smem + (size_t)s * stage_bytes);
-        const uint32_t b_base = a_base + LT_A_CHUNK;
 #pragma unroll
-        for (int kk = 0; kk < LT_BK / 16; ++kk) {
-          const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
-          const uint64_t bdesc = smem_desc_sw128(b_base + kk * 2048, LT_BOX, 1024);
-          tc_mma_f16(tmem, adesc, bdesc, idesc, (i | kk) != 0);
-        }
+        for (int kk = 0; kk < LT_BK / 16; ++kk)
+          tc_mma_f16(tmem, adesc0 + soff + (uint64_t)(kk * 2), bdesc0 + soff + (uint64_t)(kk * 128), idesc, (i | kk) != 0);
         tc_commit(&empty[s]);
+        if (++s == (uint32_t)p.stages) {
+          s = 0;
+          ph ^= 1;
+          soff = 0;
+        } else {
+          soff += stage_bytes >> 4;
+        }
       }
       if (dead) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
       timed_out = dead;
@@ -613,22 +619,29 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
       // g / v (an N=64 MMA runs at ~64 % of the N=128 rate)
       constexpr uint32_t idesc = idesc_bf16_f32(LT_BM, 128, 0, 1);
       bool dead = false;
+      // stage 0's descriptors; a stage adds its offset and a K step of 16
+      // adds 32 bytes to A and 16 rows (2 KB) to B (address field: 16-byte units)
+      const uint64_t adesc0 = smem_desc_sw128(smem_u32(smem), 16, 1024);
+      const uint64_t gvdesc0 = smem_desc_sw128(smem_u32(smem) + LT_A_CHUNK, LT_BOX, 1024);
+      uint32_t s = 0, ph = 0, soff = 0;
       for (int i = 0; i < p.chunks; ++i) {
-        const uint32_t s = i % p.stages, k = i / p.stages;
-        if (!mbar_wait(&full[s], k & 1)) {
+        if (!mbar_wait(&full[s], ph)) {
           dead = true;
           break;
         }
         tc_fence_after();
         if (i == 0) XP_TRACE_MARK(19);
-        const uint32_t a_base = smem_u32(smem + (size_t)s * stage_bytes);
 #pragma unroll
-        for (int kk = 0; kk < LT_BK / 16; ++kk) {
-          const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
-          const uint64_t gvdesc = smem_desc_sw128(a_base + LT_A_CHUNK + kk * 2048, LT_BOX, 1024);
-          tc_mma_f16(tmem, adesc, gvdesc, idesc, (i | kk) != 0);
-        }
+        for (int kk = 0; kk < LT_BK / 16; ++kk)
+          tc_mma_f16(tmem, adesc0 + soff + (uint64_t)(kk * 2), gvdesc0 + soff + (uint64_t)(kk * 128), idesc, (i | kk) != 0);
         tc_commit(&empty[s]);
+        if (++s == (uint32_t)p.stages) {
+          s = 0;
+          ph ^= 1;
+          soff = 0;
+        } else {
+          soff += stage_bytes >> 4;
+        }
       }
       if (dead) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
       timed_out = dead;
@@ -814,23 +827,29 @@ mlp_down_kernel(const __grid_constant__ CUtensorMap mapM, const __grid_constant_
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(LT_BM, p.tn, 0, 1);
       bool dead = false;
+      // stage 0's descriptors; a stage adds its offset and a K step of 16
+      // adds 32 bytes to A and 16 rows (2 KB) to B (address field: 16-byte units)
+      const uint64_t adesc0 = smem_desc_sw128(smem_u32(smem), 16, 1024);
+      const uint64_t bdesc0 = smem_desc_sw128(smem_u32(smem) + LT_A_CHUNK, LT_BOX, 1024);
+      uint32_t s = 0, ph = 0, soff = 0;
       for (int i = 0; i < nck; ++i) {
-        const uint32_t s = i % p.stages, k = i / p.stages;
-        if (!mbar_wait(&full[s], k & 1)) {
+        if (!mbar_wait(&full[s], ph)) {
           dead = true;
           break;
         }
         tc_fence_after();
         if (i == 0) XP_TRACE_MARK(32 + 7);
-        const uint32_t a_base = smem_u32(smem + (size_t)s * stage_bytes);
-        const uint32_t b_base = a_base + LT_A_CHUNK;
 #pragma unroll
-        for (int kk = 0; kk < LT_BK / 16; ++kk) {
-          const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
-          const uint64_t bdesc = smem_desc_sw128(b_base + kk * 2048, LT_BOX, 1024);
-          tc_mma_f16(tmem, adesc, bdesc, idesc, (i | kk) != 0);
-        }
+        for (int kk = 0; kk < LT_BK / 16; ++kk)
+          tc_mma_f16(tmem, adesc0 + soff + (uint64_t)(kk * 2), bdesc0 + soff + (uint64_t)(kk * 128), idesc, (i | kk) != 0);
         tc_commit(&empty[s]);
+        if (++s == (uint32_t)p.stages) {
+          s = 0;
+          ph ^= 1;
+          soff = 0;
+        } else {
+          soff += stage_bytes >> 4;
+        }
       }
       if (dead) flag_error(p.hdr, XP_DEVERR_TIMEOUT);
       timed_out = dead;

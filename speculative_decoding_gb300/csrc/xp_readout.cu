@@ -328,6 +328,9 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       bool dead = !mbar_wait_cluster(a_ready, 0);
       tc_fence_after();
       const int ksteps = (p.R + 15) / 16;
+      // slot 0's W2t descriptor; slot 1 adds the slot size (address field:
+      // 16-byte units)
+      const uint64_t bdesc0 = smem_desc_sw128(smem_u32(sB), 16, 1024);
       for (int t = 0; t < ntiles && !dead; ++t) {
         const uint32_t a = t & 1, u = t >> 1;
         if (u >= 1 && !mbar_wait_cluster(&acc_empty[a], (u - 1) & 1)) {
@@ -348,12 +351,19 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
         // a K step of 16 advances 32 bytes inside a 64-wide box.  The
         // descriptor's address field is in 16-byte units, so the steps are
         // added to the slot's descriptor directly.
-        const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + (size_t)a * RO_W2_SLOT), 16, 1024);
+        const uint64_t bdesc = bdesc0 + (uint64_t)(a * (RO_W2_SLOT >> 4));
+        if (ksteps == RO_MAX_KCH * 4) {
 #pragma unroll
-        for (int kk = 0; kk < RO_MAX_KCH * 4; ++kk) {
-          if (kk < ksteps)
+          for (int kk = 0; kk < RO_MAX_KCH * 4; ++kk)
             tc_mma_f16_ts_pair(d, tmem + RO_TMEM_A + kk * 8,
                                bdesc + (uint64_t)(((kk >> 2) * RO_W2_BOX + (kk & 3) * 32) >> 4), idesc, kk != 0);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < RO_MAX_KCH * 4; ++kk) {
+            if (kk < ksteps)
+              tc_mma_f16_ts_pair(d, tmem + RO_TMEM_A + kk * 8,
+                                 bdesc + (uint64_t)(((kk >> 2) * RO_W2_BOX + (kk & 3) * 32) >> 4), idesc, kk != 0);
+          }
         }
         tc_commit_pair(&acc_full[a], 0x3);
       }
