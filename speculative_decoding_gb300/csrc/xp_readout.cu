@@ -67,6 +67,7 @@ constexpr int RO_THREADS = (RO_WARP_BASE + 1) * 32;
 constexpr uint32_t RO_W2_BOX = 64 * RO_HALF * 2;       // 64 K x 64 vocab (8 KB)
 constexpr int RO_MAX_KCH = 8;                          // R <= 512 (K chunks of 64)
 constexpr uint32_t RO_W2_SLOT = RO_MAX_KCH * RO_W2_BOX;  // one tile's W2t half: 64 KB per CTA
+constexpr int RO_PREFETCH_TILES = 6;                   // W2t tiles pulled into L2 early (one M tile only)
 constexpr int RO_SLOTS = 2;                            // slot t % 2 holds tile t, refilled by producer t % 2
 constexpr uint32_t RO_BASE_BOX = RO_BM * 64 * 2;       // base box: 128 rows x 64 cols (16 KB)
 constexpr uint32_t RO_BASE_TILE = RO_BM * RO_BN * 2;   // 32 KB
@@ -250,6 +251,17 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
       if (lane < p.kch)
         tma_load_2d_pair(sB + (size_t)pid * RO_W2_SLOT + lane * RO_W2_BOX, &mapW2, lane * 64,
                          n0 + (int)rank * RO_HALF, leader_bar(&b_full[pid]), pol);
+      if (t == 0 && p.rows <= RO_BM) {
+        // A small batch (one M tile) leaves most SMs idle during the latent
+        // stage, and its readout CTAs are resident early: they pull the next
+        // RO_PREFETCH_TILES tiles of their W2t half into L2 meanwhile (more
+        // than that measured slower: the pulls then delay the latent stage's
+        // own reads)
+        for (int j = lane; j < RO_PREFETCH_TILES * p.kch; j += 32) {
+          const int pt = 1 + j / p.kch, bx = j - (pt - 1) * p.kch;
+          if (pt < ntiles) tma_prefetch_2d(&mapW2, bx * 64, (n_begin + pt) * RO_BN + (int)rank * RO_HALF);
+        }
+      }
       if (t == pid) pdl_wait();  // after the first tile of this slot is requested
     }
     pdl_wait();  // returns at once if already passed above
