@@ -38,6 +38,7 @@ namespace xp {
 constexpr int LT_BM = 128;                          // rows per M tile
 constexpr int LT_BK = 64;                           // K per chunk (one 128-byte swizzle row)
 constexpr int LT_THREADS = 192;                     // warp 0 TMA, warp 1 MMA, warps 2..5 workers
+constexpr int LT_UP_THREADS = 320;                  // mlp_up: warps 2..9 (two per TMEM lane quadrant)
 constexpr uint32_t LT_A_CHUNK = LT_BM * LT_BK * 2;  // 16 KB
 constexpr uint32_t LT_BOX = 64 * 64 * 2;            // one 64 x 64 bf16 box (8 KB)
 constexpr int LT_MAX_B = 16;
@@ -526,7 +527,7 @@ struct UpParams {
 // kGemm: the GEMM schedule (g and v rounded to bf16 before the SiLU, as the
 // bf16 u @ wgu_t returns them); else the in-kernel MLP (fp32 g and v)
 template <bool kGemm>
-__global__ void __launch_bounds__(LT_THREADS, 1)
+__global__ void __launch_bounds__(LT_UP_THREADS, 2)
 mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__ CUtensorMap mapWg,
               const __grid_constant__ CUtensorMap mapWu, const UpParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -656,10 +657,11 @@ mlp_up_kernel(const __grid_constant__ CUtensorMap mapUb, const __grid_constant__
     }
     tc_fence_after();
     if (threadIdx.x == 64) XP_TRACE_MARK(21);
+    // two warps per TMEM lane quadrant, one 32-column half of g and v each
     const int q = warp & 3;
     const int row = mt * LT_BM + q * 32 + lane;
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
+    {
+      const int c = (warp - 2) >> 2;
       uint32_t g[32], v[32];
       tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + c * 32, g);
       tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + 64 + c * 32, v);
@@ -957,7 +959,8 @@ namespace {
 bool g_lt_attr[64];
 int g_lt_sms[64];  // multiprocessors of each device (read with the attributes)
 
-cudaError_t launch_ex(const void* kernel_fn, dim3 grid, size_t smem, cudaStream_t stream, int cluster, void** args) {
+cudaError_t launch_ex(const void* kernel_fn, dim3 grid, size_t smem, cudaStream_t stream, int cluster, void** args,
+                      int threads = LT_THREADS) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attrs[2];
   int na = 0;
@@ -970,7 +973,7 @@ cudaError_t launch_ex(const void* kernel_fn, dim3 grid, size_t smem, cudaStream_
   attrs[na].val.programmaticStreamSerializationAllowed = 1;
   ++na;
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(LT_THREADS);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attrs;
@@ -1114,7 +1117,7 @@ xp_status launch_latent(const int64_t* blk, const int64_t* am1, const uint16_t* 
       return XP_ERR_LAUNCH;
     void* args[] = {&mapUb, &mapWg, &mapWu, &p};
     const void* up_fn = do_mlp ? (const void*)mlp_up_kernel<false> : (const void*)mlp_up_kernel<true>;
-    if (launch_ex(up_fn, dim3((unsigned)(mtiles * p.htiles)), smem, stream, 1, args) != cudaSuccess) {
+    if (launch_ex(up_fn, dim3((unsigned)(mtiles * p.htiles)), smem, stream, 1, args, LT_UP_THREADS) != cudaSuccess) {
       (void)cudaGetLastError();
       return XP_ERR_LAUNCH;
     }
