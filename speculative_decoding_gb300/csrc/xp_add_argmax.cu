@@ -22,6 +22,7 @@
 
 #include "xp_common.cuh"
 #include "xp_internal.h"
+#include "xp_ptx.cuh"
 
 namespace xp {
 
@@ -113,10 +114,10 @@ add_argmax_kernel(const uint16_t* __restrict__ base, int64_t ld_base, const uint
 #pragma unroll
     for (int w = 1; w < WARPS; ++w) ic = min(ic, s_idx[w]);
     atomicMax(&keys[row], make_key(mc, (uint32_t)ic));
-    __threadfence();
-    const unsigned int arrived = atomicAdd(&cnt[row], 1u);
+    // the arrival releases this CTA's key fold and, for the last CTA of the
+    // row, acquires every other CTA's
+    const unsigned int arrived = atom_add_acq_rel_gpu(&cnt[row], 1u);
     if (arrived == (unsigned int)nchunks - 1u) {
-      __threadfence();
       const unsigned long long k = atomicExch(&keys[row], 0ull);
       cnt[row] = 0u;
       const int64_t n = row / (B - 1), jj = row - n * (B - 1);

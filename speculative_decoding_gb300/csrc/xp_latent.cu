@@ -349,8 +349,7 @@ proj_mix_kernel(const __grid_constant__ CUtensorMap mapWlat, const __grid_consta
     int ok = 1;
     if (lane == 0) {
       fence_proxy_async_global();
-      __threadfence();
-      atomicAdd(&p.cnt[2 * tile], 1u);
+      (void)atom_add_acq_rel_gpu(&p.cnt[2 * tile], 1u);  // releases this CTA's stored partial
       const unsigned long long t0 = globaltimer();
       while (ld_acquire_gpu(&p.cnt[2 * tile]) < (uint32_t)p.S) {
         if (globaltimer() - t0 > kWaitLimitNs) {

@@ -223,6 +223,14 @@ __device__ __forceinline__ void cp_async_wait_group_n(int n) {
 }
 
 // acquire load of a global counter (GPU scope)
+// atomic add with acquire-release semantics at GPU scope: this thread's
+// earlier writes are visible before the add, and the writes of the threads
+// whose adds came before it are visible after it
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

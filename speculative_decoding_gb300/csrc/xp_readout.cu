@@ -498,9 +498,9 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
     // error bit is set).
     if (row_ok) {
       if (bidx >= 0 && !dead) atomicMax(&p.keys[row], make_key(best, (uint32_t)bidx));
-      __threadfence();
-      if (atomicAdd(&p.rcnt[row], 1u) == 2u * (uint32_t)p.per - 1u) {
-        __threadfence();
+      // the arrival releases this fold and, for the row's last arrival,
+      // acquires every other one
+      if (atom_add_acq_rel_gpu(&p.rcnt[row], 1u) == 2u * (uint32_t)p.per - 1u) {
         const unsigned long long k = atomicExch(&p.keys[row], 0ull);
         p.rcnt[row] = 0u;
         const int64_t idx = (int64_t)key_index(k);
