@@ -21,12 +21,19 @@
 //               partials of its own column slice in a fixed order, adds the
 //               hidden cache, applies the causal mixer and writes u (fp32)
 //               and bf16(u).
-//   mlp_up    : ub @ Wg and ub @ Wu as two TMEM accumulators over the same A
-//               tile; the epilogue applies SiLU(g) * v and rounds to bf16.
+//   mlp_up    : ub @ Wg and ub @ Wu as one N=128 MMA per K step into two
+//               64-column halves of a TMEM accumulator; eight epilogue warps
+//               (two per TMEM lane quadrant) apply SiLU(g) * v and round to
+//               bf16.
 //   mlp_down  : m @ Wd with the H-long reduction split over a cluster; the
 //               reduction adds the fp32 residual u and writes bf16 latents for
 //               slots 1..B-1.
-// The three launches are chained with programmatic dependent launch.
+// The three launches are chained with programmatic dependent launch.  One
+// thread issues each kernel's MMAs, and anything else in its loop delays them
+// (a barrier wait costs it about as much as three MMAs), so the issue loops
+// carry the ring's stage and phase in running counters and add constants to
+// per-stage descriptors instead of dividing by the stage count and rebuilding
+// the descriptors for every chunk.
 #include "xp_common.cuh"
 #include "xp_internal.h"
 #include "xp_ptx.cuh"
@@ -37,7 +44,7 @@ namespace xp {
 
 constexpr int LT_BM = 128;                          // rows per M tile
 constexpr int LT_BK = 64;                           // K per chunk (one 128-byte swizzle row)
-constexpr int LT_THREADS = 192;                     // warp 0 TMA, warp 1 MMA, warps 2..5 workers
+constexpr int LT_THREADS = 192;                     // warp 0 TMA, warp 1 MMA, warps 2..5 workers (proj_mix, mlp_down)
 constexpr int LT_UP_THREADS = 320;                  // mlp_up: warps 2..9 (two per TMEM lane quadrant)
 constexpr uint32_t LT_A_CHUNK = LT_BM * LT_BK * 2;  // 16 KB
 constexpr uint32_t LT_BOX = 64 * 64 * 2;            // one 64 x 64 bf16 box (8 KB)
