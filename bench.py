@@ -139,13 +139,18 @@ class ClockSampler:
         while self.proc and not self.samples and time.time() < t_end:
             time.sleep(0.05)
 
-    def __exit__(self, *a):
+    def stop(self):
+        """End the sampling (the samples taken so far stay)."""
         if self.proc:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=2)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+            self.proc = None
+
+    def __exit__(self, *a):
+        self.stop()
 
     def summary(self, t0, t1):
         inside = [p for (t, p) in self.samples if t0 - 0.25 <= t <= t1 + 0.25] or [p for (_, p) in self.samples]
@@ -323,6 +328,9 @@ def run_gb300(args, rank, world, local_rank):
         if xpress.read_error(ws) != 0:
             raise RuntimeError("device-side error bits set during the timed passes")
         clocks = clk.summary(t0, t1)
+        # the clocks are those of the timed passes: the sampler (an nvidia-smi
+        # process polling the driver) stops before the other legs
+        clk.stop()
 
         # ---- the dominant kernel alone: the readout with its fused epilogue
         lat = torch.empty((N, B - 1, R), dtype=torch.bfloat16, device=device)
