@@ -364,6 +364,9 @@ readout_argmax_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_co
         // descriptor's address field is in 16-byte units, so the steps are
         // added to the slot's descriptor directly.
         const uint64_t bdesc = bdesc0 + (uint64_t)(a * (RO_W2_SLOT >> 4));
+        // R = 512 fills the tile's K: its MMAs go out without a per-MMA
+        // predicate (whatever else the single issuing thread does between
+        // MMAs delays them)
         if (ksteps == RO_MAX_KCH * 4) {
 #pragma unroll
           for (int kk = 0; kk < RO_MAX_KCH * 4; ++kk)
